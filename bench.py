@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""Throughput of the W4A16 MoE expert layer on GB300.
+
+One step = one pass of the whole layer over one synthetic canvas: routing
+(top-k + softmax + per-expert pair lists), the grouped gate_up GEMM with the
+gated GELU, the grouped down GEMM and the fixed-order combine, all through the
+library's C ABI on device-resident inputs.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload canvas256] [--impl ours|reference]
+
+Under torchrun every rank runs its own canvas on its own GPU (independent
+problems, no collective on the data path): weak scaling; value = tokens of all
+ranks / max-over-ranks time.  `--impl reference` times the CPU oracle (the
+method's plain fp64 definition) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE expert-layer tokens/s at 256-token canvas; achieved HBM GB/s vs GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gate_up_gemm_canvas256.txt")
+DOMINANT_SRC = os.path.join(ROOT, "w4a16_moe_expert_router_gb300", "csrc", "gemm_mma.cu")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--workload", default="canvas256")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=2000)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------ distributed ----
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    group = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        group = dist.group.WORLD
+    return rank, world, local, group
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- helpers ----
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(path: str) -> str:
+    with open(path, "rb") as fh:
+        return hashlib.sha256(fh.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged since the capture."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    vals = {}
+    with open(PROFILE_TRAFFIC) as fh:
+        for ln in fh:
+            if ":" in ln:
+                k, v = ln.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != source_hash(DOMINANT_SRC):
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- our arm ----
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    from w4a16_moe_expert_router_gb300 import binding as B
+    from w4a16_moe_expert_router_gb300 import build as libbuild
+    from w4a16_moe_expert_router_gb300 import runtime, synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py (--impl ours) needs a CUDA GPU")
+    libbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = synth.WORKLOADS[args.workload]
+    layers = wl.layers
+    seed = rank  # every rank denoises its own canvas
+    x_bits = synth.make_x(wl, seed)
+    logits = [synth.make_logits(wl, seed, layer=l) for l in range(layers)]
+    # two copies of every layer's weights alternate between steps (each > L2 already)
+    copies = 2 if layers == 1 else 1
+    weights, gammas, touched = [], [], []
+    for l in range(layers):
+        w = synth.make_weights(wl, 0, layer=l)
+        gu, dn = runtime.prepare_host(wl, w)
+        for _ in range(copies):
+            weights.append(runtime.PreparedWeights(torch.from_numpy(gu).to(dev), torch.from_numpy(dn).to(dev)))
+        gammas.append(runtime.to_device_f32(synth.make_gamma(wl, 0, layer=l), dev) if wl.rmsnorm else None)
+        del w, gu, dn
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    buf = runtime.alloc_buffers(wl, device=dev, stream=stream)
+    x = runtime.to_device_x(x_bits, dev)
+    lg = [runtime.to_device_f32(a, dev) for a in logits]
+    outs = [torch.empty((wl.tokens, wl.hidden), dtype=torch.float16, device=dev) for _ in range(2)]
+
+    L = B.lib()
+    import ctypes
+    sh = buf.shape
+    r = buf.routing.c()
+    ws_ptr, ws_n = buf.workspace.data_ptr(), buf.workspace.numel()
+    wstructs = [B.Weights(w.gate_up.data_ptr(), w.down.data_ptr()) for w in weights]
+    shp, rp = ctypes.byref(sh), ctypes.byref(r)
+
+    def layer_calls(l, src, dst, w_i, evs=None):
+        """route, gate_up, down, combine of layer l; events between the calls if given."""
+        if evs is not None:
+            evs[0].record(stream)
+        st = L.moe_w4a16_route(shp, lg[l].data_ptr(), rp, ws_ptr, ws_n, sptr)
+        if evs is not None:
+            evs[1].record(stream)
+        st |= L.moe_w4a16_gate_up(shp, src.data_ptr(), rp, ctypes.byref(wstructs[w_i]), ws_ptr, ws_n, sptr)
+        if evs is not None:
+            evs[2].record(stream)
+        st |= L.moe_w4a16_down(shp, rp, ctypes.byref(wstructs[w_i]), ws_ptr, ws_n, sptr)
+        if evs is not None:
+            evs[3].record(stream)
+        g = gammas[l]
+        st |= L.moe_w4a16_combine(shp, rp, None if g is None else g.data_ptr(), 1e-6, dst.data_ptr(), ws_ptr,
+                                  ws_n, sptr)
+        if evs is not None:
+            evs[4].record(stream)
+        if st:
+            raise RuntimeError(f"library call failed with status {st}")
+
+    def step(i, evs=None):
+        """One step = the whole layer stack over the canvas."""
+        src = x
+        for l in range(layers):
+            dst = outs[l % 2]
+            w_i = l * copies + (i % copies)
+            layer_calls(l, src, dst, w_i, evs[l] if evs is not None else None)
+            src = dst
+
+    # routing statistics for the algorithmic byte count (per layer: experts touched)
+    for l in range(layers):
+        B.moe_w4a16_route(sh, lg[l], buf.routing, buf.workspace, stream)
+        off = buf.routing.expert_offsets.cpu().numpy()
+        touched.append(int(np.count_nonzero(np.diff(off))))
+    d, f, g1, g2 = wl.hidden, wl.inter, wl.group_gate_up, wl.group_down
+    gu_bytes_e = 2 * f * d // 2 + 2 * f * (d // g1) * 4
+    dn_bytes_e = d * f // 2 + d * (f // g2) * 4
+    gu_bytes = [t * gu_bytes_e for t in touched]
+    layer_bytes = sum(t * (gu_bytes_e + dn_bytes_e) for t in touched)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(layers)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        t_start.record(stream)
+        for i in range(K):
+            step(i, evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if B.moe_w4a16_read_error(buf.workspace, stream) != B.OK:
+        raise RuntimeError("a device-side wait timed out during the timed region")
+    max_ms = max_over_ranks(elapsed_ms, world, dev)
+
+    # per-kernel averages over the timed region
+    parts = np.zeros((layers, 4))
+    for i in range(K):
+        for l in range(layers):
+            e = evs[i][l]
+            for j in range(4):
+                parts[l, j] += e[j].elapsed_time(e[j + 1])
+    parts /= K
+    route_us, gate_us, down_us, comb_us = (parts.mean(0) * 1e3).tolist()
+
+    tokens_total = wl.tokens * K * world
+    value = tokens_total / (max_ms / 1e3)
+    ms_per_step = max_ms / K
+    peak, peak_src = measured_peak()
+    achieved = (sum(gu_bytes) / layers) / (gate_us * 1e-6) / 1e9
+    layer_gbs = layer_bytes / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the public API: pinned host buffers, copies inside the timed region
+    x_host = torch.from_numpy(x_bits.view(np.float16)).pin_memory()
+    lg_host = [torch.from_numpy(a).pin_memory() for a in logits]
+    out_host = torch.empty((wl.tokens, wl.hidden), dtype=torch.float16).pin_memory()
+    x_in = torch.empty_like(x)
+    lg_in = [torch.empty_like(a) for a in lg]
+    KE = max(1, min(args.e2e_steps, K))
+
+    def e2e_step(i):
+        x_in.copy_(x_host, non_blocking=True)
+        src = x_in
+        for l in range(layers):
+            lg_in[l].copy_(lg_host[l], non_blocking=True)
+            dst = outs[l % 2]
+            B.moe_w4a16_route(sh, lg_in[l], buf.routing, buf.workspace, stream)
+            wts = weights[l * copies + (i % copies)]
+            B.moe_w4a16_forward(sh, src, buf.routing, wts.gate_up, wts.down, gammas[l], 1e-6, dst, buf.workspace,
+                                stream)
+            src = dst
+        out_host.copy_(src, non_blocking=True)
+
+    for i in range(min(10, KE)):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(KE):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    h2d = x_bits.nbytes + sum(a.nbytes for a in logits)
+    d2h = wl.tokens * wl.hidden * 2
+
+    result = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": wl.name, "tokens": wl.tokens, "hidden": wl.hidden, "inter": wl.inter,
+            "experts": wl.experts, "top_k": wl.top_k, "group_gate_up": wl.group_gate_up,
+            "group_down": wl.group_down, "layers": layers, "rmsnorm": wl.rmsnorm,
+            "experts_touched_per_layer": touched,
+            "l2": f"inputs larger than L2: {layer_bytes / layers / 1e6:.0f} MB of expert weights per layer "
+                  f"vs 129 MB L2" + ("; two weight copies alternate between steps" if copies == 2 else ""),
+            "parallelism": f"replicas x{world} (one canvas per GPU)",
+        },
+        "hbm_gbs": layer_gbs,
+        "hbm_frac_of_peak": layer_gbs / peak,
+        "kernel_us": {"route": route_us, "gate_up": gate_us, "down": down_us, "combine": comb_us},
+        "roofline": {
+            "kernel": "expert_gemm_kernel<0> (gate_up grouped dequant GEMM)",
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": peak_src, "traffic": profiled_traffic(),
+            "algorithmic_bytes_per_launch": sum(gu_bytes) / layers,
+        },
+        "e2e": {"value": wl.tokens * KE * world / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE},
+        "gpu_launches": K * layers * 5,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl)
+    return result
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+class OracleCase:
+    """Seeded inputs of one layer of the workload, generated once, for the CPU oracle."""
+
+    def __init__(self, wl, layer=0):
+        from w4a16_moe_expert_router_gb300 import synth
+        self.wl = wl
+        self.x = synth.make_x(wl, 0)
+        self.lg = synth.make_logits(wl, 0, layer=layer)
+        self.w = synth.make_weights(wl, 0, layer=layer)
+        self.gamma = synth.make_gamma(wl, 0, layer=layer) if wl.rmsnorm else None
+
+    def time_tokens(self, tokens, nthreads):
+        """Seconds the oracle takes for routing + experts + combine of the given tokens."""
+        import numpy as np
+
+        import oracle
+        wl = self.wl
+        sel = np.zeros(wl.tokens, np.uint8)
+        sel[np.asarray(list(tokens))] = 1
+        t0 = time.perf_counter()
+        idx, tw = oracle.route(self.lg, wl.top_k)
+        oracle.forward(self.x, idx, tw, self.w, group_gate_up=wl.group_gate_up, group_down=wl.group_down,
+                       activation=wl.activation, gamma=self.gamma, eps=1e-6, token_sel=sel, nthreads=nthreads)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(wl):
+    nth = os.cpu_count() or 1
+    secs = OracleCase(wl).time_tokens(range(wl.tokens), nth)
+    per_step = wl.layers  # one canvas through the whole stack
+    return {"value": wl.tokens / (secs * per_step), "unit": "tokens/s", "cores": nth, "kind": "oracle",
+            "sample": f"one full {wl.name} layer ({wl.tokens} tokens: routing, fp64 dequantised expert FFNs, "
+                      f"combine), {nth} threads" + (f"; scaled by {per_step} layers per step" if per_step > 1 else "")}
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, one token of the canvas per step, on the host cores."""
+    if rank != 0:
+        return None
+    from w4a16_moe_expert_router_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    nth = os.cpu_count() or 1
+    case = OracleCase(wl)
+    for i in range(args.warmup):
+        case.time_tokens([i % wl.tokens], nth)
+    budget_s, t0, done, spent = 120.0, time.perf_counter(), 0, 0.0
+    for i in range(args.steps):
+        spent += case.time_tokens([i % wl.tokens], nth) * wl.layers
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    value = done / spent
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": done,
+        "warmup": args.warmup, "ms_per_step": 1e3 * spent / done, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "tokens": wl.tokens, "hidden": wl.hidden, "inter": wl.inter,
+                   "experts": wl.experts, "top_k": wl.top_k, "layers": wl.layers},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nth, "kind": "oracle",
+                         "sample": "one token of the canvas per step (its routing, its k experts dequantised "
+                                   f"in fp64, the combine), {nth} threads"
+                                   + (f"; stopped after {done} of {args.steps} steps at the {budget_s:.0f} s budget"
+                                      if done < args.steps else "")},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        # host-only: rank 0 times the oracle, the other ranks exit without work
+        rank = int(os.environ.get("RANK", "0"))
+        res = run_reference(args, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    rank, world, local, _ = dist_setup()
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,210 @@
+/*
+ * moe_w4a16.h -- C ABI of the W4A16 MoE expert layer for GB300 (sm_103a).
+ *
+ * The layer (per denoising step of a block-diffusion LM; model card
+ * "srswti/axe-diffusion-ksl-xe", sections "what the model is" and "the kernels
+ * we built"):
+ *   1. route:   each of T tokens picks its top-k of E experts from fp32 router
+ *               logits; the k selected logits are softmax-normalised;
+ *   2. expert:  each (token, expert) pair runs the expert's gated-GELU FFN
+ *               h = gelu(Wg x) * (Wu x),  y = Wd h,  with Wg|Wu|Wd stored as
+ *               asymmetric uint4 codes with an fp16 scale and zero-point per
+ *               group along the contraction dim, w = (q - z) * s, dequantised
+ *               inside the GEMM ("the kernels we built": the GEMM reads packed
+ *               nibbles and dequantises inline);
+ *   3. combine: out[t] = sum over router ranks r = 0..k-1, in rank order, of
+ *               w[t][r] * y[t][r], in fp32 with no atomics ("the kernels we
+ *               built": fixed-order combine instead of index_add_), optionally
+ *               followed by an fp32 RMSNorm ("the kernels we built": fused
+ *               RMSNorm).
+ * The weight format follows the model card's "requirements" paragraph
+ * (dg-w4a16-v1: two nibbles per byte; gate_up_proj grouped along the
+ * contraction dim; down_proj grouped at 64 because its contraction dim, 704, is
+ * not a multiple of 128).
+ *
+ * Conventions for every call:
+ *   - Device pointers are allocated and owned by the caller; the library
+ *     allocates nothing, never synchronises the host (except
+ *     moe_w4a16_read_error), and launches only on the given stream
+ *     (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *   - Shapes and pointers are validated on the host before anything is
+ *     launched; on any status other than MOE_W4A16_OK nothing was launched
+ *     and no output was written.  The library never reads device data to
+ *     validate it: out-of-range device contents (e.g. an expert id >= E in a
+ *     caller-built routing) are the caller's responsibility.
+ *   - fp16 values travel as uint16_t bit patterns (IEEE binary16).
+ *   - Every device pointer must be 16-byte aligned.
+ *   - Calls sharing one workspace must not overlap in time (same stream, or
+ *     ordered by events); calls with separate workspaces are independent.
+ *   - Results are bit-identical from run to run for the same inputs and shape:
+ *     no floating-point atomics are used and every reduction has a fixed order.
+ */
+#ifndef MOE_W4A16_H
+#define MOE_W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_W4A16_API __attribute__((visibility("default")))
+#else
+#define MOE_W4A16_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_W4A16_OK = 0,
+  MOE_W4A16_ERR_NULL = 1,      /* a required pointer is NULL */
+  MOE_W4A16_ERR_SHAPE = 2,     /* shape outside the supported set (see moe_w4a16_shape) */
+  MOE_W4A16_ERR_ALIGN = 3,     /* a device pointer is not 16-byte aligned */
+  MOE_W4A16_ERR_WORKSPACE = 4, /* workspace smaller than moe_w4a16_workspace_bytes() */
+  MOE_W4A16_ERR_CUDA = 5,      /* a CUDA runtime call or kernel launch failed */
+  MOE_W4A16_ERR_DEVICE = 6,    /* current device is not a compute capability 10.3 GPU */
+  MOE_W4A16_ERR_TIMEOUT = 7,   /* a device-side wait ran out (reported by moe_w4a16_read_error) */
+  MOE_W4A16_ERR_VALUE = 8      /* host data out of range (a code > 15, a scale or zero the kernels cannot hold) */
+} moe_w4a16_status;
+
+/* Layer shape.
+ *   tokens        T >= 0 (T = 0 is an OK no-op)
+ *   hidden        d, a multiple of 128
+ *   inter         f (expert FFN width), a multiple of 64
+ *   experts       E, 1..256
+ *   top_k         k, 1..min(E, 8)
+ *   group_gate_up g1 in {32, 64, 128}, dividing d: quantisation group of gate_up_proj along d
+ *   group_down    g2 in {32, 64, 128}, dividing f: quantisation group of down_proj along f
+ *   activation    0 = GELU tanh form 0.5a(1+tanh(sqrt(2/pi)(a+0.044715a^3))), 1 = GELU erf form
+ * T*k must not exceed 2^22. */
+typedef struct {
+  int32_t tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation;
+} moe_w4a16_shape;
+
+/* Expert weights of one layer, in the prepared layout written by
+ * moe_w4a16_prepare (see there); device pointers, read only.
+ *   gate_up  moe_w4a16_prepared_bytes(shape, MOE_W4A16_GATE_UP) bytes
+ *   down     moe_w4a16_prepared_bytes(shape, MOE_W4A16_DOWN) bytes */
+typedef struct {
+  const uint8_t* gate_up;
+  const uint8_t* down;
+} moe_w4a16_weights;
+
+/* Routing of one canvas, written by moe_w4a16_route, read by moe_w4a16_forward
+ * (device pointers):
+ *   topk_idx        int32 [T][k]   expert ids in router-rank order (rank 0 = largest logit)
+ *   topk_w          fp32  [T][k]   softmax over the k selected logits
+ *   expert_offsets  int32 [E+1]    pairs of expert e are pair_list[offsets[e] .. offsets[e+1])
+ *   pair_list       int32 [T*k]    pair ids p = t*k + r grouped by expert, p ascending within an expert */
+typedef struct {
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* expert_offsets;
+  int32_t* pair_list;
+} moe_w4a16_routing;
+
+#define MOE_W4A16_GATE_UP 0
+#define MOE_W4A16_DOWN 1
+
+/* Bytes of device workspace that moe_w4a16_route and moe_w4a16_forward need for
+ * this shape (0 on an invalid shape).  The workspace holds the intermediate
+ * activations h (fp16 [T*k][f]) and per-pair expert outputs (fp32 [T*k][d]) plus
+ * a small header (error word, work counters).  It must be initialised once with
+ * moe_w4a16_workspace_init before its first use; later calls leave it ready. */
+MOE_W4A16_API size_t moe_w4a16_workspace_bytes(const moe_w4a16_shape* shape);
+
+/* Clears the workspace header (error word and work counters) on `stream`. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Routing (step 1): top-k, softmax over the selected logits, and the per-expert
+ * pair lists.  Ties between equal logits go to the lower expert index (compared
+ * as fp32 values, so -0 ties +0).  Logits must be finite; NaN or infinite
+ * logits give unspecified (but in-bounds) routing.
+ *   logits  fp32 [T][E], device, read only
+ *   out     the four routing arrays, device, written */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_route(const moe_w4a16_shape* shape, const float* logits, const moe_w4a16_routing* out,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Expert FFNs and combine (steps 2 and 3).
+ *   x           fp16 [T][d], device, read only
+ *   routing     as written by moe_w4a16_route (read only)
+ *   weights     prepared weights of this layer
+ *   norm_gamma  fp32 [d] or NULL; when given, out = fp16(gamma * u / sqrt(mean(u^2) + norm_eps))
+ *               with u the fp32 combine result; when NULL, out = fp16(u)
+ *   out         fp16 [T][d], device, written; must not overlap x or the workspace
+ * Rounding: fp16 results are rounded to nearest even. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_forward(const moe_w4a16_shape* shape, const uint16_t* x, const moe_w4a16_routing* routing,
+                                   const moe_w4a16_weights* weights, const float* norm_gamma, float norm_eps,
+                                   uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The three launches of moe_w4a16_forward, callable one by one on the same
+ * stream in this order (same arguments and rules as moe_w4a16_forward; e.g. to
+ * time each step or to interleave other work):
+ *   moe_w4a16_gate_up  expert gate_up GEMMs with the gated GELU folded into the
+ *                      epilogue: h = gelu(Wg x) * (Wu x) for every (token, expert)
+ *                      pair -> fp16 rows in the workspace, ordered by expert
+ *   moe_w4a16_down     expert down GEMMs: y = Wd h -> fp32 rows in the workspace,
+ *                      one per pair p = t*k + r
+ *   moe_w4a16_combine  out[t] = fp16(sum_r w[t][r] y[t*k+r]) in rank order, with the
+ *                      optional RMSNorm */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_gate_up(const moe_w4a16_shape* shape, const uint16_t* x,
+                                                 const moe_w4a16_routing* routing, const moe_w4a16_weights* weights,
+                                                 void* workspace, size_t workspace_bytes, void* stream);
+MOE_W4A16_API moe_w4a16_status moe_w4a16_down(const moe_w4a16_shape* shape, const moe_w4a16_routing* routing,
+                                              const moe_w4a16_weights* weights, void* workspace,
+                                              size_t workspace_bytes, void* stream);
+MOE_W4A16_API moe_w4a16_status moe_w4a16_combine(const moe_w4a16_shape* shape, const moe_w4a16_routing* routing,
+                                                 const float* norm_gamma, float norm_eps, uint16_t* out,
+                                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Copies the workspace's sticky error word to the host after synchronising
+ * `stream`: MOE_W4A16_OK, or MOE_W4A16_ERR_TIMEOUT if a device-side wait of an
+ * earlier call gave up (its outputs are then invalid).  Cleared by
+ * moe_w4a16_workspace_init. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_read_error(const void* workspace, size_t workspace_bytes, void* stream,
+                                      moe_w4a16_status* device_status);
+
+/* ---- host-side weight helpers (no GPU needed) ---------------------------- */
+
+/* Canonical packing of uint4 codes (dg-w4a16-v1 style, model card
+ * "requirements": two nibbles per byte): codes [rows][K] with values 0..15 ->
+ * packed [rows][K/2], byte b of a row holding column 2b in its low nibble and
+ * column 2b+1 in its high nibble.  K must be even.  ERR_VALUE if a code > 15. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_pack(const uint8_t* codes, int64_t rows, int64_t K, uint8_t* packed);
+
+/* Inverse of moe_w4a16_pack. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_unpack(const uint8_t* packed, int64_t rows, int64_t K, uint8_t* codes);
+
+/* Bytes of the prepared layout of one projection of all E experts:
+ * exactly the canonical bytes (packed nibbles + fp16 scale + fp16 zero). */
+MOE_W4A16_API size_t moe_w4a16_prepared_bytes(const moe_w4a16_shape* shape, int32_t which);
+
+/* Rearranges one projection of all E experts from the canonical layout into the
+ * kernels' prepared layout (a byte permutation; no value changes).  Host memory.
+ *   which   MOE_W4A16_GATE_UP: rows R = 2f (rows [0,f) gate, [f,2f) up), K = d, g = g1
+ *           MOE_W4A16_DOWN:    rows R = d, K = f, g = g2
+ *   q       canonical packed codes [E][R][K/2]
+ *   scale   fp16 bits [E][R][K/g]
+ *   zero    fp16 bits [E][R][K/g]
+ *   out     moe_w4a16_prepared_bytes(shape, which) bytes
+ * The prepared layout is private to this library version: a stream of 64-column
+ * stages per block of 128 GEMM rows, each stage holding the block's scale/zero
+ * pairs for the groups that start in it followed by the codes in the order the
+ * kernels' dequantiser consumes them.
+ * ERR_VALUE if a scale is not finite or |scale| > 32, or a zero-point lies outside
+ * [0, 16] (the kernels' fp16 dequantisation is exact only in that range). */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_prepare(const moe_w4a16_shape* shape, int32_t which, const uint8_t* q,
+                                   const uint16_t* scale, const uint16_t* zero, uint8_t* out);
+
+/* Inverse of moe_w4a16_prepare (for checking a prepared buffer). */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_unprepare(const moe_w4a16_shape* shape, int32_t which, const uint8_t* prepared,
+                                     uint8_t* q, uint16_t* scale, uint16_t* zero);
+
+/* Static description of a status code (never NULL). */
+MOE_W4A16_API const char* moe_w4a16_status_string(moe_w4a16_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_W4A16_H */

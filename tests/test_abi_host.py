@@ -1,0 +1,183 @@
+"""Host-only tests of the C-ABI library: it loads, exports what the header
+declares, validates shapes and pointers before touching a GPU, and its host
+weight helpers (pack/unpack, prepare/unprepare) are exact permutations."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from w4a16_moe_expert_router_gb300 import binding as B
+from w4a16_moe_expert_router_gb300 import build as libbuild
+from w4a16_moe_expert_router_gb300 import synth, runtime
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    libbuild.build()
+    return B.lib()
+
+
+def _header_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"^MOE_W4A16_API\s+[\w\s\*]+?\b(moe_w4a16_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    names = _header_functions()
+    assert len(names) >= 11
+    raw = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert set(names) == set(B.EXPORTED)
+
+
+def test_status_strings():
+    for code in range(9):
+        assert B.moe_w4a16_status_string(code)
+    assert B.moe_w4a16_status_string(99) == "unknown status"
+
+
+VALID = dict(tokens=16, hidden=256, inter=128, experts=8, top_k=2, group_gate_up=64, group_down=64)
+
+
+def _shape(**kw):
+    d = dict(VALID)
+    d.update(kw)
+    return B.make_shape(**d)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(hidden=192), dict(hidden=64), dict(inter=96), dict(experts=0), dict(experts=257), dict(top_k=0),
+    dict(top_k=9), dict(experts=4, top_k=5), dict(group_gate_up=48), dict(group_gate_up=16),
+    dict(group_down=128, inter=192), dict(activation=2), dict(tokens=-1), dict(tokens=1 << 20, top_k=8),
+])
+def test_invalid_shapes_rejected(bad):
+    sh = _shape(**bad)
+    assert B.moe_w4a16_workspace_bytes(sh) == 0
+    assert B.moe_w4a16_prepared_bytes(sh, B.GATE_UP) == 0
+    L = B.lib()
+    r = B.Routing(16, 16, 16, 16)
+    assert L.moe_w4a16_route(ctypes.byref(sh), 16, ctypes.byref(r), 16, 1 << 30, None) == B.ERR_SHAPE
+    w = B.Weights(16, 16)
+    assert L.moe_w4a16_forward(ctypes.byref(sh), 16, ctypes.byref(r), ctypes.byref(w), None, 1e-6, 16, 16,
+                               1 << 30, None) == B.ERR_SHAPE
+
+
+def test_workspace_size_covers_intermediates():
+    sh = _shape()
+    T, k, d, f = 16, 2, 256, 128
+    assert B.moe_w4a16_workspace_bytes(sh) >= 256 + T * k * f * 2 + T * k * d * 4
+
+
+def test_pointer_and_workspace_validation_before_any_launch():
+    L = B.lib()
+    sh = _shape()
+    ws = B.moe_w4a16_workspace_bytes(sh)
+    good = B.Routing(4096, 4096, 4096, 4096)
+    w = B.Weights(4096, 4096)
+    fwd = lambda x, r, wt, out, wsp, wsb, gamma=None, eps=1e-6: L.moe_w4a16_forward(
+        ctypes.byref(sh), x, ctypes.byref(r), ctypes.byref(wt), gamma, eps, out, wsp, wsb, None)
+    assert fwd(None, good, w, 4096, 4096, ws) == B.ERR_NULL
+    assert fwd(4096, B.Routing(4096, None, 4096, 4096), w, 4096, 4096, ws) == B.ERR_NULL
+    assert fwd(4096, good, B.Weights(4096, None), 4096, 4096, ws) == B.ERR_NULL
+    assert fwd(4104, good, w, 4096, 4096, ws) == B.ERR_ALIGN
+    assert fwd(4096, good, w, 4096, 4096, ws, gamma=4100) == B.ERR_ALIGN
+    assert fwd(4096, good, w, 4096, 4096, ws - 1) == B.ERR_WORKSPACE
+    assert fwd(4096, good, w, 4096, 4096, ws, eps=-1.0) == B.ERR_VALUE
+    rt = lambda lg, r, wsb: L.moe_w4a16_route(ctypes.byref(sh), lg, ctypes.byref(r), 4096, wsb, None)
+    assert rt(None, good, ws) == B.ERR_NULL
+    assert rt(4097, good, ws) == B.ERR_ALIGN
+    assert rt(4096, B.Routing(4096, 4096, 4104, 4096), ws) == B.ERR_ALIGN
+    assert rt(4096, good, 100) == B.ERR_WORKSPACE
+    assert L.moe_w4a16_route(ctypes.byref(sh), 4096, None, 4096, ws, None) == B.ERR_NULL
+
+
+def test_zero_tokens_is_a_no_op():
+    L = B.lib()
+    sh = _shape(tokens=0)
+    r = B.Routing(None, None, None, None)
+    w = B.Weights(None, None)
+    assert L.moe_w4a16_route(ctypes.byref(sh), None, ctypes.byref(r), None, 0, None) == B.OK
+    assert L.moe_w4a16_forward(ctypes.byref(sh), None, ctypes.byref(r), ctypes.byref(w), None, 1e-6, None, None, 0,
+                               None) == B.OK
+
+
+def test_pack_unpack_round_trip_all_bytes():
+    packed = np.arange(256, dtype=np.uint8).reshape(4, 64)
+    codes = B.moe_w4a16_unpack(packed)
+    assert codes.shape == (4, 128)
+    assert np.array_equal(B.moe_w4a16_pack(codes), packed)
+    assert codes[2, 70] == 3 and codes[2, 71] == 10      # byte 163 = 0xA3 sits at row 2, column 35
+    row = B.moe_w4a16_unpack(np.array([[0xA3]], np.uint8))
+    assert list(row[0]) == [3, 10]
+
+
+def test_pack_rejects_codes_above_15():
+    with pytest.raises(B.MoeW4A16Error) as e:
+        B.moe_w4a16_pack(np.array([[3, 16]], np.uint8))
+    assert e.value.status == B.ERR_VALUE
+
+
+@pytest.mark.parametrize("g1,g2,d,f,E", [(64, 64, 256, 128, 3), (32, 32, 256, 192, 2), (128, 64, 384, 64, 2),
+                                         (128, 128, 256, 256, 1)])
+def test_prepare_unprepare_round_trip(g1, g2, d, f, E):
+    wl = synth.Workload("t", 4, d, f, E, 1, g1, g2)
+    w = synth.make_weights(wl, seed=g1 + g2 + d)
+    sh = runtime.shape_of(wl)
+    for which, q, s, z in ((B.GATE_UP, "gate_up_q", "gate_up_scale", "gate_up_zero"),
+                           (B.DOWN, "down_q", "down_scale", "down_zero")):
+        prep = B.moe_w4a16_prepare(sh, which, w[q], w[s], w[z])
+        assert prep.nbytes == w[q].nbytes + w[s].nbytes + w[z].nbytes == B.moe_w4a16_prepared_bytes(sh, which)
+        q2, s2, z2 = B.moe_w4a16_unprepare(sh, which, prep, w[q].shape, w[s].shape)
+        assert np.array_equal(q2, w[q]) and np.array_equal(s2, w[s]) and np.array_equal(z2, w[z])
+
+
+def test_prepared_word_layout_matches_documented_fragment_order():
+    """First stage of block 0 of expert 0 of gate_up: (scale, zero) of 128 GEMM rows,
+    then words [tile][lane][k16 step]; GEMM row r of tile m is gate row 8m+r (r<8)
+    or up row f+8m+r-8."""
+    wl = synth.WORKLOADS["tiny"]
+    w = synth.make_weights(wl, seed=9)
+    sh = runtime.shape_of(wl)
+    prep = B.moe_w4a16_prepare(sh, B.GATE_UP, w["gate_up_q"], w["gate_up_scale"], w["gate_up_zero"])
+    codes = B.moe_w4a16_unpack(w["gate_up_q"])[0]          # [2f][d]
+    f = wl.inter
+    row = lambda m, r: 8 * m + r if r < 8 else f + 8 * m + r - 8
+    sz = prep[:512].view(np.uint16).reshape(128, 2)
+    for r in range(128):
+        assert sz[r, 0] == w["gate_up_scale"][0, row(r // 16, r % 16), 0]
+        assert sz[r, 1] == w["gate_up_zero"][0, row(r // 16, r % 16), 0]
+    words = prep[512:512 + 4096].view(np.uint32).reshape(8, 32, 4)
+    for m in (0, 3, 7):
+        for lane in (0, 5, 31):
+            for kk in (0, 3):
+                g, t = lane // 4, lane % 4
+                c = 16 * kk + 2 * t
+                want = [codes[row(m, g), c], codes[row(m, g + 8), c], codes[row(m, g), c + 8],
+                        codes[row(m, g + 8), c + 8], codes[row(m, g), c + 1], codes[row(m, g + 8), c + 1],
+                        codes[row(m, g), c + 9], codes[row(m, g + 8), c + 9]]
+                wd = int(words[m, lane, kk])
+                assert [(wd >> (4 * i)) & 15 for i in range(8)] == want
+
+
+def test_prepare_rejects_out_of_range_scale_and_zero():
+    wl = synth.WORKLOADS["tiny"]
+    w = synth.make_weights(wl)
+    sh = runtime.shape_of(wl)
+    s = w["gate_up_scale"].copy()
+    s[0, 0, 0] = np.float16(40.0).view(np.uint16)
+    with pytest.raises(B.MoeW4A16Error) as e:
+        B.moe_w4a16_prepare(sh, B.GATE_UP, w["gate_up_q"], s, w["gate_up_zero"])
+    assert e.value.status == B.ERR_VALUE
+    z = w["gate_up_zero"].copy()
+    z[1, 2, 3] = np.float16(-0.5).view(np.uint16)
+    with pytest.raises(B.MoeW4A16Error):
+        B.moe_w4a16_prepare(sh, B.GATE_UP, w["gate_up_q"], w["gate_up_scale"], z)

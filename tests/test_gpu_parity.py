@@ -1,0 +1,171 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Bars (fixed by the layer's specification of this library):
+  routing       topk_idx, expert_offsets and pair_list equal element for element;
+  gating        topk_w within 1e-6 relative;
+  output        max |gpu - oracle| <= 2e-2 and ||gpu - oracle||_F / ||oracle||_F <= 1e-3,
+                the GPU's fp16 output against the oracle's unrounded fp64 value;
+  determinism   repeated runs bit-identical.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from w4a16_moe_expert_router_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 2e-2
+REL_FROB = 1e-3
+W_REL = 1e-6
+NCPU = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module")
+def rt():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from w4a16_moe_expert_router_gb300 import build as libbuild
+    libbuild.build()
+    from w4a16_moe_expert_router_gb300 import runtime
+    return runtime
+
+
+def _gpu_layer(rt, wl, x, lg, w, gamma=None, eps=1e-6, repeats=1):
+    dw = rt.upload_weights(wl, w)
+    buf = rt.alloc_buffers(wl, tokens=x.shape[0])
+    xd, ld = rt.to_device_x(x), rt.to_device_f32(lg)
+    gd = None if gamma is None else rt.to_device_f32(gamma)
+    outs = []
+    for _ in range(repeats):
+        rt.run_layer(buf, xd, ld, dw, gd, eps)
+        outs.append(buf.out.clone())
+    torch.cuda.synchronize()
+    from w4a16_moe_expert_router_gb300 import binding as B
+    assert B.moe_w4a16_read_error(buf.workspace) == B.OK
+    r = buf.routing
+    routing = (r.topk_idx.cpu().numpy(), r.topk_w.cpu().numpy(), r.expert_offsets.cpu().numpy(),
+               r.pair_list.cpu().numpy())
+    return routing, [o.cpu().numpy() for o in outs]
+
+
+def _check_routing(lg, k, E, routing):
+    idx_g, w_g, off_g, pl_g = routing
+    idx_o, w_o = oracle.route(lg, k)
+    off_o, pl_o = oracle.permute(idx_o, E)
+    assert np.array_equal(idx_g, idx_o)
+    assert np.array_equal(off_g, off_o)
+    assert np.array_equal(pl_g[:len(pl_o)], pl_o)
+    assert np.all(np.abs(w_g.astype(np.float64) - w_o) <= W_REL * np.abs(w_o))
+    return idx_o, w_o
+
+
+def _check_out(out_gpu, ref, rows=None):
+    g = out_gpu.astype(np.float64)
+    if rows is not None:
+        g, ref = g[rows], ref[rows]
+    assert np.all(np.isfinite(g))
+    err = np.abs(g - ref)
+    rel = np.linalg.norm(g - ref) / np.linalg.norm(ref)
+    assert err.max() <= MAX_ABS, (err.max(), rel)
+    assert rel <= REL_FROB, (err.max(), rel)
+    return err.max(), rel
+
+
+def _full_case(rt, wl, seed=0, tokens=None, sel=None):
+    x = synth.make_x(wl, seed, tokens)
+    lg = synth.make_logits(wl, seed, tokens=tokens)
+    w = synth.make_weights(wl, seed)
+    routing, (out,) = _gpu_layer(rt, wl, x, lg, w)
+    idx, tw = _check_routing(lg, wl.top_k, wl.experts, routing)
+    ref = oracle.forward(x, idx, tw, w, group_gate_up=wl.group_gate_up, group_down=wl.group_down,
+                         activation=wl.activation, token_sel=sel, nthreads=NCPU)
+    rows = None if sel is None else np.nonzero(sel)[0]
+    return _check_out(out, ref, rows)
+
+
+def test_tiny_layer_all_tokens(rt):
+    _full_case(rt, synth.WORKLOADS["tiny"])
+
+
+@pytest.mark.parametrize("tokens", [1, 3, 17])
+def test_tiny_ragged_token_counts(rt, tokens):
+    _full_case(rt, synth.WORKLOADS["tiny"], seed=tokens, tokens=tokens)
+
+
+@pytest.mark.parametrize("wl", [
+    synth.Workload("chunks", 300, 256, 128, 4, 2, 64, 64),              # ~150 pairs per expert: 3 token chunks
+    synth.Workload("g32", 40, 256, 192, 8, 3, 32, 32),                 # two groups per stage, 3 gate blocks
+    synth.Workload("g128", 33, 384, 128, 6, 2, 128, 128, activation=1),  # group spans two stages, erf GELU
+    synth.Workload("e256", 40, 128, 64, 256, 8, 64, 32),              # max experts and top-k, mostly empty experts
+    synth.Workload("k1", 70, 256, 64, 16, 1, 128, 64),
+], ids=lambda w: w.name)
+def test_shape_variants(rt, wl):
+    _full_case(rt, wl, seed=5)
+
+
+def test_canvas64_full_size(rt):
+    _full_case(rt, synth.WORKLOADS["canvas64"])
+
+
+def test_canvas256_full_size(rt):
+    _full_case(rt, synth.WORKLOADS["canvas256"])
+
+
+def test_zipf1024_skewed_full_size(rt):
+    wl = synth.WORKLOADS["zipf1024"]
+    lg = synth.make_logits(wl)
+    idx, _ = oracle.route(lg, wl.top_k)
+    # every token routed to the hottest expert is checked, plus a spread of others
+    hot = np.nonzero((idx == 0).any(1))[0]
+    assert len(hot) > 600
+    sel = np.zeros(wl.tokens, np.uint8)
+    sel[hot[:: max(1, len(hot) // 96)]] = 1
+    sel[:: 16] = 1
+    _full_case(rt, wl, sel=sel)
+
+
+def test_canvas256_bit_identical_over_10_runs(rt):
+    wl = synth.WORKLOADS["canvas256"]
+    x, lg, w = synth.make_x(wl, 3), synth.make_logits(wl, 3), synth.make_weights(wl, 3)
+    _, outs = _gpu_layer(rt, wl, x, lg, w, repeats=10)
+    for o in outs[1:]:
+        assert np.array_equal(o.view(np.uint16), outs[0].view(np.uint16))
+
+
+def test_stack30_teacher_forced_per_layer(rt):
+    """30 layers on a 256-token canvas, each output RMS-normalised (gamma ~ N(1, 0.1))
+    and fed to the next layer.  Layer l is checked against the oracle run on the
+    GPU's own fp16 input to that layer (teacher forcing): free-running fp16 error
+    grows through the quadratic gated activation, so only per-layer parity is a
+    property of the kernels."""
+    wl = synth.WORKLOADS["stack30"]
+    from w4a16_moe_expert_router_gb300 import binding as B
+    buf = rt.alloc_buffers(wl)
+    x_bits = synth.make_x(wl)
+    xd = rt.to_device_x(x_bits)
+    sel = np.zeros(wl.tokens, np.uint8)
+    sel[::8] = 1
+    rows = np.nonzero(sel)[0]
+    worst = 0.0
+    for layer in range(wl.layers):
+        lg = synth.make_logits(wl, layer=layer)
+        w = synth.make_weights(wl, layer=layer)
+        gamma = synth.make_gamma(wl, layer=layer)
+        dw = rt.upload_weights(wl, w)
+        out = torch.empty_like(buf.out)
+        rt.run_layer(buf, xd, rt.to_device_f32(lg), dw, rt.to_device_f32(gamma), 1e-6, out=out)
+        torch.cuda.synchronize()
+        idx, tw = oracle.route(lg, wl.top_k)
+        assert np.array_equal(buf.routing.topk_idx.cpu().numpy(), idx)
+        ref = oracle.forward(x_bits, idx, tw, w, group_gate_up=64, group_down=64, gamma=gamma, eps=1e-6,
+                             token_sel=sel, nthreads=NCPU)
+        _, rel = _check_out(out.cpu().numpy(), ref, rows)
+        worst = max(worst, rel)
+        x_bits = out.cpu().numpy().view(np.uint16).copy()
+        xd = out
+        del dw
+    assert B.moe_w4a16_read_error(buf.workspace) == B.OK

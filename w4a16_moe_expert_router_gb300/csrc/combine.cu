@@ -1,0 +1,101 @@
+// combine.cu -- fixed-order weighted combine of the k expert outputs of each
+// token, with an optional fused RMSNorm.
+//
+// Model card "srswti/axe-diffusion-ksl-xe", "the kernels we built": the weighted
+// combine uses a fixed-order reduction instead of index_add_, because a 1-ulp
+// difference from atomics can flip a block-diffusion acceptance threshold; and
+// RMSNorm collapses into a single launch.  Here one CTA owns one token row:
+//   u[i]   = w[t][0] y[t*k][i] + ... + w[t][k-1] y[t*k+k-1][i]   (fp32, rank order, fused multiply-adds)
+//   out[i] = fp16(u[i])                                         without gamma
+//   out[i] = fp16(gamma[i] * u[i] / sqrt(mean(u^2) + eps))       with gamma
+// The sum of squares uses a fixed tree (per-thread in index order, butterfly
+// inside each warp, then the warps in order), so the result is bit-identical
+// from run to run.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxVec = 8;  // float4 per thread: d <= 8192
+
+template <bool kNorm>
+__global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restrict__ topk_w,
+                                                           const float* __restrict__ y, int d, int k,
+                                                           const float* __restrict__ gamma, float eps,
+                                                           uint16_t* __restrict__ out) {
+  __shared__ float warp_ss[kThreads / 32];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int n4 = d >> 2;
+  float wr[kMaxTopK];
+#pragma unroll
+  for (int r = 0; r < kMaxTopK; ++r) wr[r] = r < k ? topk_w[static_cast<size_t>(t) * k + r] : 0.f;
+  const float4* y4 = reinterpret_cast<const float4*>(y) + static_cast<size_t>(t) * k * n4;
+  float4 u[kMaxVec];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxVec; ++j) {
+    const int i4 = tid + kThreads * j;
+    if (i4 < n4) {
+      float4 v = y4[i4];
+      float4 acc = make_float4(wr[0] * v.x, wr[0] * v.y, wr[0] * v.z, wr[0] * v.w);
+#pragma unroll
+      for (int r = 1; r < kMaxTopK; ++r) {
+        if (r < k) {
+          v = y4[static_cast<size_t>(r) * n4 + i4];
+          acc.x = fmaf(wr[r], v.x, acc.x);
+          acc.y = fmaf(wr[r], v.y, acc.y);
+          acc.z = fmaf(wr[r], v.z, acc.z);
+          acc.w = fmaf(wr[r], v.w, acc.w);
+        }
+      }
+      u[j] = acc;
+      if (kNorm) {
+        ss = fmaf(acc.x, acc.x, ss);
+        ss = fmaf(acc.y, acc.y, ss);
+        ss = fmaf(acc.z, acc.z, ss);
+        ss = fmaf(acc.w, acc.w, ss);
+      }
+    }
+  }
+  float scale = 1.f;
+  if (kNorm) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((tid & 31) == 0) warp_ss[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) tot += warp_ss[w];
+    scale = 1.f / sqrtf(tot / static_cast<float>(d) + eps);
+  }
+  uint2* o2 = reinterpret_cast<uint2*>(out + static_cast<size_t>(t) * d);
+  const float4* g4 = reinterpret_cast<const float4*>(gamma);
+#pragma unroll
+  for (int j = 0; j < kMaxVec; ++j) {
+    const int i4 = tid + kThreads * j;
+    if (i4 < n4) {
+      float4 v = u[j];
+      if (kNorm) {
+        const float4 g = g4[i4];
+        v = make_float4(g.x * (v.x * scale), g.y * (v.y * scale), g.z * (v.z * scale), g.w * (v.w * scale));
+      }
+      const __half2 lo = __floats2half2_rn(v.x, v.y);
+      const __half2 hi = __floats2half2_rn(v.z, v.w);
+      o2[i4] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Dims& s, const float* topk_w, const float* y, const float* gamma, float eps,
+                           uint16_t* out, cudaStream_t st) {
+  if (gamma) combine_kernel<true><<<s.T, kThreads, 0, st>>>(topk_w, y, s.d, s.k, gamma, eps, out);
+  else combine_kernel<false><<<s.T, kThreads, 0, st>>>(topk_w, y, s.d, s.k, nullptr, eps, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
