@@ -200,6 +200,42 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_prepare(const moe_w4a16_shape* shape, i
 MOE_W4A16_API moe_w4a16_status moe_w4a16_unprepare(const moe_w4a16_shape* shape, int32_t which, const uint8_t* prepared,
                                      uint8_t* q, uint16_t* scale, uint16_t* zero);
 
+/* ---- allocation-free forward ---------------------------------------------
+ *
+ * moe_w4a16_forward_noalloc computes exactly what moe_w4a16_forward computes
+ * (the gate_up and down GEMMs and the combine, on a routing written by
+ * moe_w4a16_route), but keeps its scratch memory in a static device array built
+ * into the library instead of a caller-provided workspace, and allocates nothing.
+ * The pages describe no counterpart to this call; it exists for callers that
+ * cannot obtain device memory of their own -- for example a plugin running
+ * inside a host application whose memory manager owns the whole device heap
+ * and forbids side allocations, or a latency-critical serving loop that must
+ * not call cudaMalloc because an allocation can synchronise the device and
+ * stall the work already queued on it.
+ *
+ *   - The array holds MOE_W4A16_NOALLOC_SCRATCH_BYTES (24 MiB) and is reserved
+ *     on every GPU that loads the library until the process exits.
+ *   - A shape whose moe_w4a16_workspace_bytes() exceeds that size is rejected
+ *     with MOE_W4A16_ERR_WORKSPACE before anything is launched (a 256-token
+ *     canvas with d = 2048, f = 704 and top-8 needs about 20 MB and fits; a
+ *     1024-token batch of that layer does not).
+ *   - The first call on a device performs a one-time set-up on that device (it
+ *     looks up the array's device address and sets kernel attributes); make
+ *     that first call before capturing any stream into a CUDA graph.
+ *   - Every call on a device uses the same array: calls whose GPU work may
+ *     overlap (other streams, concurrently launched graphs) race with each
+ *     other and give undefined results.  Each call clears the array's work
+ *     counters when it starts; the rest keeps the last call's contents until
+ *     overwritten.
+ *   - A device-side wait that runs out is not reported (the error word sits in
+ *     the static array); such a call's output is invalid.
+ * Arguments are those of moe_w4a16_forward, without the workspace. */
+#define MOE_W4A16_NOALLOC_SCRATCH_BYTES ((size_t)24 << 20)
+MOE_W4A16_API moe_w4a16_status moe_w4a16_forward_noalloc(const moe_w4a16_shape* shape, const uint16_t* x,
+                                                         const moe_w4a16_routing* routing,
+                                                         const moe_w4a16_weights* weights, const float* norm_gamma,
+                                                         float norm_eps, uint16_t* out, void* stream);
+
 /* Static description of a status code (never NULL). */
 MOE_W4A16_API const char* moe_w4a16_status_string(moe_w4a16_status status);
 

@@ -24,7 +24,9 @@ GATE_UP, DOWN = 0, 1
 
 EXPORTED = ("moe_w4a16_workspace_bytes", "moe_w4a16_workspace_init", "moe_w4a16_route", "moe_w4a16_forward",
             "moe_w4a16_gate_up", "moe_w4a16_down", "moe_w4a16_combine", "moe_w4a16_read_error", "moe_w4a16_pack", "moe_w4a16_unpack", "moe_w4a16_prepared_bytes",
-            "moe_w4a16_prepare", "moe_w4a16_unprepare", "moe_w4a16_status_string")
+            "moe_w4a16_prepare", "moe_w4a16_unprepare", "moe_w4a16_status_string", "moe_w4a16_forward_noalloc")
+
+NOALLOC_SCRATCH_BYTES = 24 << 20  # MOE_W4A16_NOALLOC_SCRATCH_BYTES
 
 
 class MoeW4A16Error(RuntimeError):
@@ -76,6 +78,9 @@ def lib() -> ctypes.CDLL:
             L.moe_w4a16_down.restype = st
             L.moe_w4a16_combine.argtypes = [P(Shape), P(Routing), vp, ctypes.c_float, vp, vp, sz, vp]
             L.moe_w4a16_combine.restype = st
+            L.moe_w4a16_forward_noalloc.argtypes = [P(Shape), vp, P(Routing), P(Weights), vp, ctypes.c_float, vp,
+                                                    vp]
+            L.moe_w4a16_forward_noalloc.restype = st
             L.moe_w4a16_read_error.argtypes = [vp, sz, vp, P(ctypes.c_int)]
             L.moe_w4a16_read_error.restype = st
             L.moe_w4a16_pack.argtypes = [vp, i64, i64, vp]
@@ -170,6 +175,17 @@ def moe_w4a16_forward(shape: Shape, x, routing: RoutingBuffers, gate_up, down, n
     _check(lib().moe_w4a16_forward(ctypes.byref(shape), _dptr(x), ctypes.byref(r), ctypes.byref(w),
                                    _dptr(norm_gamma), float(norm_eps), _dptr(out), _dptr(workspace),
                                    _nbytes(workspace), _stream(stream)), "moe_w4a16_forward")
+
+
+def moe_w4a16_forward_noalloc(shape: Shape, x, routing: RoutingBuffers, gate_up, down, norm_gamma,
+                              norm_eps: float, out, stream=None) -> None:
+    """The forward pass with the library's static scratch array instead of a
+    workspace, for callers that cannot allocate device memory (see the header)."""
+    r = routing.c()
+    w = Weights(_dptr(gate_up), _dptr(down))
+    _check(lib().moe_w4a16_forward_noalloc(ctypes.byref(shape), _dptr(x), ctypes.byref(r), ctypes.byref(w),
+                                           _dptr(norm_gamma), float(norm_eps), _dptr(out), _stream(stream)),
+           "moe_w4a16_forward_noalloc")
 
 
 def moe_w4a16_gate_up(shape: Shape, x, routing: RoutingBuffers, gate_up, down, workspace, stream=None) -> None:
