@@ -30,7 +30,7 @@ if ROOT not in sys.path:
 METRIC = "MoE expert-layer tokens/s at 256-token canvas; achieved HBM GB/s vs GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gate_up_gemm_canvas256.txt")
-DOMINANT_SRC = os.path.join(ROOT, "w4a16_moe_expert_router_gb300", "csrc", "gemm_mma.cu")
+DOMINANT_SRC = os.path.join(ROOT, "w4a16_moe_expert_router_gb300", "csrc", "gemm_tc.cu")
 
 
 def log(*a):
@@ -354,7 +354,7 @@ def run_ours(args, rank, world, local):
         "hbm_frac_of_peak": layer_gbs / peak,
         "kernel_us": {"route": route_us, "gate_up": gate_us, "down": down_us, "combine": comb_us},
         "roofline": {
-            "kernel": "expert_gemm_kernel<0> (gate_up grouped dequant GEMM)",
+            "kernel": "expert_gemm_tc_kernel<0> (gate_up grouped dequant GEMM, tcgen05)",
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "peak_source": peak_src, "traffic": profiled_traffic(),
             "algorithmic_bytes_per_launch": sum(gu_bytes) / layers,

@@ -140,32 +140,35 @@ def test_prepare_unprepare_round_trip(g1, g2, d, f, E):
         assert np.array_equal(q2, w[q]) and np.array_equal(s2, w[s]) and np.array_equal(z2, w[z])
 
 
-def test_prepared_word_layout_matches_documented_fragment_order():
+def test_prepared_word_layout_matches_documented_order():
     """First stage of block 0 of expert 0 of gate_up: (scale, zero) of 128 GEMM rows,
-    then words [tile][lane][k16 step]; GEMM row r of tile m is gate row 8m+r (r<8)
-    or up row f+8m+r-8."""
+    then words [half][GEMM row][4]; GEMM row r is gate row r (r < 64) or up row
+    f + r - 64; nibble i of word w holds column 32*half + 8w + (0,2,4,6,1,3,5,7)[i]."""
     wl = synth.WORKLOADS["tiny"]
     w = synth.make_weights(wl, seed=9)
     sh = runtime.shape_of(wl)
     prep = B.moe_w4a16_prepare(sh, B.GATE_UP, w["gate_up_q"], w["gate_up_scale"], w["gate_up_zero"])
     codes = B.moe_w4a16_unpack(w["gate_up_q"])[0]          # [2f][d]
     f = wl.inter
-    row = lambda m, r: 8 * m + r if r < 8 else f + 8 * m + r - 8
+    row = lambda r: r if r < 64 else f + r - 64
     sz = prep[:512].view(np.uint16).reshape(128, 2)
     for r in range(128):
-        assert sz[r, 0] == w["gate_up_scale"][0, row(r // 16, r % 16), 0]
-        assert sz[r, 1] == w["gate_up_zero"][0, row(r // 16, r % 16), 0]
-    words = prep[512:512 + 4096].view(np.uint32).reshape(8, 32, 4)
-    for m in (0, 3, 7):
-        for lane in (0, 5, 31):
-            for kk in (0, 3):
-                g, t = lane // 4, lane % 4
-                c = 16 * kk + 2 * t
-                want = [codes[row(m, g), c], codes[row(m, g + 8), c], codes[row(m, g), c + 8],
-                        codes[row(m, g + 8), c + 8], codes[row(m, g), c + 1], codes[row(m, g + 8), c + 1],
-                        codes[row(m, g), c + 9], codes[row(m, g + 8), c + 9]]
-                wd = int(words[m, lane, kk])
-                assert [(wd >> (4 * i)) & 15 for i in range(8)] == want
+        assert sz[r, 0] == w["gate_up_scale"][0, row(r), 0]
+        assert sz[r, 1] == w["gate_up_zero"][0, row(r), 0]
+    words = prep[512:512 + 4096].view(np.uint32).reshape(2, 128, 4)
+    order = (0, 2, 4, 6, 1, 3, 5, 7)
+    for hf in (0, 1):
+        for r in (0, 5, 63, 64, 127):
+            for wi in (0, 3):
+                c0 = 32 * hf + 8 * wi
+                wd = int(words[hf, r, wi])
+                assert [(wd >> (4 * i)) & 15 for i in range(8)] == [codes[row(r), c0 + order[i]] for i in range(8)]
+    # the second stage of the down projection starts after the first stage's 512 + 4096 bytes
+    dn = B.moe_w4a16_prepare(sh, B.DOWN, w["down_q"], w["down_scale"], w["down_zero"])
+    dcodes = B.moe_w4a16_unpack(w["down_q"])[0]             # [d][f]
+    words2 = dn[2 * (512 + 4096) - 4096: 2 * (512 + 4096)].view(np.uint32).reshape(2, 128, 4)
+    wd = int(words2[1, 7, 1])
+    assert [(wd >> (4 * i)) & 15 for i in range(8)] == [dcodes[7, 64 + 32 + 8 + order[i]] for i in range(8)]
 
 
 def test_prepare_rejects_out_of_range_scale_and_zero():

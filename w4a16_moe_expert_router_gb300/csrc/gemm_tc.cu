@@ -1,0 +1,694 @@
+// gemm_tc.cu -- grouped W4A16 expert GEMMs with inline dequantisation on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// Model card "srswti/axe-diffusion-ksl-xe", "the kernels we built": the GEMM
+// reads packed nibbles and dequantises inline, so HBM carries real 4-bit
+// traffic; one launch covers all experts; the activation is folded into the
+// first GEMM's epilogue.  Two launches of one kernel template do the work:
+//   gate_up:  a[p][n] = sum_k Wgu[e][n][k] x[t(p)][k]  (64 gate + 64 up rows per item)
+//             h[pos(p)][j] = gelu(a[p][j]) * a[p][f+j]  -> fp16, rows in expert-sorted order
+//   down:     y[p][i] = sum_j Wd[e][i][j] h[pos(p)][j]   -> fp32, rows by pair id p = t*k + r
+//
+// Arithmetic: each weight is formed as w = fp16(fp16(q - z) * s): the offset
+// removal and q - z are exact in fp16 (unless |q - z| >= 8 needs a 12th
+// significand bit), the product with the scale is rounded once, and the tensor
+// core multiplies w with the fp16 activations into an fp32 accumulator that stays
+// in tensor memory for the whole contraction.
+//
+// Roles of the persistent CTA (two per SM, 256 tensor-memory columns each; work
+// items = (expert, 128-row block, chunk of <= 32 tokens) taken from a global
+// counter, each item self-contained so results do not depend on which CTA ran
+// it; the CTA's stages are numbered t = 0, 1, ... across its items):
+//   warp 0      producer: per 64-column stage, one 1-D bulk copy of the block's
+//               stream segment (scale/zero pairs + codes) and 2-D TMA loads
+//               (128-byte swizzle, 16-row boxes) of the item's activation rows
+//               into a ring of eight shared-memory slots (mbarrier complete_tx);
+//   warps 1-2   MMA issuers (warp 1 also allocates tensor memory): one lane
+//               each; issuer i issues the tcgen05.mma of k16 steps 2i and 2i+1 of
+//               every stage into its own fp32 accumulator (A = dequantised
+//               weights in TMEM, B = activations in SMEM, M = 128 rows, N =
+//               tokens rounded up to 16).  Issuing an MMA of this skinny shape
+//               occupies the issuing thread for ~50-90 cycles whatever N is, so
+//               two issuers share that cost; each commits once per stage
+//               (releasing the slot and the TMEM stage) and once per item;
+//   warps 3-6   dequantisers, one warp per TMEM lane quadrant: each thread owns
+//               one GEMM row and writes the row's 64 weights of a stage into one
+//               of four TMEM stages (one tcgen05.st of 32 columns); at an item's
+//               last stage the same warps read the row's two accumulators
+//               (tcgen05.ld, added in a fixed order) and run the epilogue -- the
+//               gated GELU through a shared-memory exchange of the up rows, or
+//               the fp32 row stores of the down projection -- while the issuers
+//               already fill the other accumulator set.
+// Every wait is bounded: on expiry the CTA records MOE_W4A16_ERR_TIMEOUT in the
+// workspace and all roles leave their loops, drain what is in flight and free
+// tensor memory.  No split-K and no atomics on data.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kGroups = 1;                     // dequant groups (four warps each, one per lane quadrant)
+constexpr int kDqWarps = 4 * kGroups;
+constexpr int kIssuers = 2;                    // MMA issuers: k16 steps {0,1} and {2,3} of every stage
+constexpr int kFirstDqWarp = 1 + kIssuers;
+constexpr int kThreads = (kFirstDqWarp + kDqWarps) * 32;  // 224
+constexpr int kCtasPerSm = 2;
+constexpr int kAStages = 4;                    // TMEM stages of dequantised weights
+constexpr int kSlots = 8;                      // shared-memory stages in flight per CTA
+constexpr int kDBufs = 2;                      // accumulator sets (items alternate)
+constexpr int kNMax = kChunkN;                 // 32 tokens per item
+constexpr int kACols = 32;                     // 128 rows x 64 fp16 = 32 columns
+constexpr int kDCols = kIssuers * kNMax;       // the issuers' fp32 accumulators of one item
+constexpr int kDCol0 = kAStages * kACols;      // first accumulator column
+constexpr int kTmemCols = 256;
+static_assert(kDCol0 + kDBufs * kDCols <= kTmemCols, "TMEM budget");
+static_assert(kNMax == 32, "the dequant warps hold 32 accumulator columns");
+static_assert(kSlots % kAStages == 0, "stage t uses slot t % kSlots and TMEM stage t % kAStages");
+constexpr int kBBoxRows = 16;                  // TMA box: 64 columns x 16 rows = 2 KiB
+constexpr int kBBytes = kNMax * 128;           // 4 KiB, 128B-swizzled K-major
+constexpr int kSzBytes = kBlockRows * 4;       // 512: (scale, zero) of 128 rows for one group
+constexpr int kCodeBytes = kBlockRows * kStageK / 2;  // 4096
+constexpr int kCodeOff = kBBytes + 2 * kSzBytes;      // codes always land here
+constexpr int kSlotBytes = 10240;                     // multiple of 1024
+static_assert(kCodeOff + kCodeBytes <= kSlotBytes && kSlotBytes % 1024 == 0, "slot layout");
+constexpr int kXchStride = kNMax + 4;          // floats per exchanged row (bank-conflict padding)
+constexpr int kXchBytes = kGroups * 64 * kXchStride * 4;  // one exchange area per group
+constexpr int kHeaderBytes = 2048;
+constexpr int kRingOff = (kHeaderBytes + kXchBytes + 1023) / 1024 * 1024;
+constexpr int kSmemBytes = 1024 + kRingOff + kSlots * kSlotBytes;  // +1024 for alignment
+
+struct TcArgs {
+  const uint8_t* w;         // prepared stream of the projection, all experts
+  int64_t expert_bytes;     // stream bytes per expert
+  int64_t block_bytes;      // stream bytes per 128-row block
+  int nblocks;              // blocks per expert
+  int K;                    // contraction length (multiple of 64)
+  int g;                    // quantisation group along K (32, 64 or 128)
+  const int32_t* offsets;   // [E+1]
+  const int32_t* pair_list; // [T*k]
+  int E;
+  uint16_t* h_out;          // gate_up output [T*k][f]
+  float* y_out;             // down output [T*k][d]
+  int f, d, act;
+  int32_t* err;
+  int32_t* counter;
+  int32_t* counter_to_reset;
+};
+
+// Shared-memory header (at the 1024-aligned base of dynamic shared memory).
+struct __align__(8) TcHeader {
+  uint64_t slot_full[kSlots];
+  uint64_t slot_empty[kSlots];
+  uint64_t a_full[kAStages];    // a TMEM stage is written (4 warps)
+  uint64_t d_full[kDBufs];      // an item's accumulators are final (one commit per issuer)
+  uint64_t d_free[kDBufs];      // the epilogue has read them (4 warps)
+  uint64_t drain;
+  uint64_t xch_ready[kGroups];  // the 2 up-row warps of a group have written their rows
+  uint64_t xch_done[kGroups];   // the 2 gate-row warps of a group have read them
+  int slot_item[kSlots];
+  int slot_stage[kSlots];
+  int slot_seq[kSlots];         // the item's sequence number within this CTA
+  uint32_t tmem_base;
+  int abort;
+  int prefix[kMaxExperts + 1];
+};
+static_assert(sizeof(TcHeader) <= kHeaderBytes, "header fits");
+
+// Groups whose first column lies in stage s (g is 32, 64 or 128).
+__device__ __forceinline__ int groups_in_stage(int s, int g) {
+  return g == 32 ? 2 : (((s * kStageK) & (g - 1)) == 0 ? 1 : 0);
+}
+
+__device__ __forceinline__ int expert_of(int item, const int* prefix, int E) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {  // largest e with prefix[e] <= item
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= item) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Work item -> (expert, 128-row block, token chunk); the chunk varies fastest,
+// so concurrent items of a busy expert share weight blocks in L2.
+__device__ __forceinline__ void decode_item(int item, const int* prefix, const TcArgs& a, int& expert, int& blk,
+                                            int& n_cnt, int& pos0) {
+  const int e = expert_of(item, prefix, a.E);
+  const int n_e = a.offsets[e + 1] - a.offsets[e];
+  const int nch = (n_e + kChunkN - 1) / kChunkN;
+  const int r = item - prefix[e];
+  const int c = r % nch;
+  expert = e;
+  blk = r / nch;
+  n_cnt = min(kChunkN, n_e - kChunkN * c);
+  pos0 = a.offsets[e] + kChunkN * c;
+}
+
+// --- tcgen05 wrappers ---------------------------------------------------------
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16 (fp16 inputs, fp32 accumulate)
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor of kind::f16: fp16 A and B (K-major), fp32 D, M = 128, N = n.
+__device__ __forceinline__ uint32_t f16_idesc(int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kBlockRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// 8 codes of one row (nibbles in column order 0,2,4,6,1,3,5,7) -> four f16x2 weights
+// w = fp16(fp16(q - z) * s) for columns (k, k+1), (k+2, k+3), (k+4, k+5), (k+6, k+7).
+// (1024 + q) and (64 + q) come from OR-ing exponent bits onto the nibbles; one fp16
+// add removes the offset exactly, one subtract forms q - z (exact unless |q - z| >= 8
+// needs a 12th significand bit) and one multiply rounds the product once.
+__device__ __forceinline__ void dequant_row8(uint32_t w, __half2 z, __half2 s, uint32_t* out) {
+  const uint32_t w8 = w >> 8;
+  const __half2 m1024 = bits_h2(0xe400e400u), m64 = bits_h2(0xd400d400u);
+  out[0] = h2_bits(__hmul2(__hsub2(__hadd2(bits_h2(and_or(w, 0x000f000fu, 0x64006400u)), m1024), z), s));
+  out[1] = h2_bits(__hmul2(__hsub2(__hadd2(bits_h2(and_or(w, 0x00f000f0u, 0x54005400u)), m64), z), s));
+  out[2] = h2_bits(__hmul2(__hsub2(__hadd2(bits_h2(and_or(w8, 0x000f000fu, 0x64006400u)), m1024), z), s));
+  out[3] = h2_bits(__hmul2(__hsub2(__hadd2(bits_h2(and_or(w8, 0x00f000f0u, 0x54005400u)), m64), z), s));
+}
+
+__device__ __forceinline__ float gelu(float a, int act) {
+  if (act == 1) return 0.5f * a * (1.f + erff(a * 0.70710678118654752f));
+  return 0.5f * a * (1.f + tanhf(0.79788456080286536f * (a + 0.044715f * a * a * a)));
+}
+
+// Bounded wait by one thread that also gives up once another role of this CTA has.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const TcArgs& a, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait_sleep(bar, parity, kSuspendNs)) {
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicExch(a.err, kStatusTimeout);
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// Warp-uniform bounded wait: every lane polls the barrier (so each acquires the
+// phase), the warp leaves together once all lanes have seen it complete, and the
+// decision to give up is lane 0's, broadcast, so a warp never splits before a
+// warp-collective instruction.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const TcArgs& a, volatile int* abort) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSuspendNs))) return true;
+    int give_up = 0;
+    if ((threadIdx.x & 31) == 0) {
+      give_up = *abort != 0;
+      if (!give_up && global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicExch(a.err, kStatusTimeout);
+        *abort = 1;
+        give_up = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+  }
+}
+
+template <int kEpi>  // 0: gate_up with GeGLU epilogue, 1: down projection
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    expert_gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap bmap) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  TcHeader& H = *reinterpret_cast<TcHeader*>(smem);
+  float* xch_all = reinterpret_cast<float*>(smem + kHeaderBytes);
+  uint8_t* ring = smem + kRingOff;
+  volatile int* abort = &H.abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (blockIdx.x == 0 && tid == 0) *a.counter_to_reset = 0;
+  if (tid == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_addr(&H.slot_full[i]), 1);
+      mbar_init(smem_addr(&H.slot_empty[i]), 4 + kIssuers);  // the stage's 4 dequant warps + 2 commits
+    }
+    for (int i = 0; i < kAStages; ++i) mbar_init(smem_addr(&H.a_full[i]), 4);
+    for (int i = 0; i < kGroups; ++i) {
+      mbar_init(smem_addr(&H.xch_ready[i]), 2);
+      mbar_init(smem_addr(&H.xch_done[i]), 2);
+    }
+    for (int i = 0; i < kDBufs; ++i) {
+      mbar_init(smem_addr(&H.d_full[i]), kIssuers);
+      mbar_init(smem_addr(&H.d_free[i]), 4);
+    }
+    mbar_init(smem_addr(&H.drain), kIssuers);
+    H.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&H.tmem_base)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (warp == 2) {  // items per expert = blocks * ceil(n_e / 32); exclusive scan, 8 experts per lane
+    int loc[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = lane * 8 + j;
+      loc[j] = sum;
+      if (e < a.E) sum += a.nblocks * ((a.offsets[e + 1] - a.offsets[e] + kChunkN - 1) / kChunkN);
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (lane * 8 + j < a.E) H.prefix[lane * 8 + j] = incl - sum + loc[j];
+    if (lane == 31) H.prefix[a.E] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = H.tmem_base;
+  const int total = H.prefix[a.E];
+  const int nst = a.K / kStageK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&bmap) : "memory");
+    int t = 0, seq = 0, sentinels = 0;
+    uint32_t issued_mask = 0;   // slots whose last phase carried copies
+    uint32_t issued_par = 0;    // parity of that phase, one bit per slot
+    bool ok = true;
+    while (ok && sentinels < kGroups) {
+      int item = 0;
+      if (lane == 0) item = atomicAdd(a.counter, 1);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      const bool done = item >= total;
+      int e = 0, blk = 0, n_cnt = 0, pos0 = 0;
+      if (!done) decode_item(item, H.prefix, a, e, blk, n_cnt, pos0);
+      const int nbox = (n_cnt + kBBoxRows - 1) / kBBoxRows;
+      const uint8_t* wsrc =
+          a.w + static_cast<int64_t>(e) * a.expert_bytes + static_cast<int64_t>(blk) * a.block_bytes;
+      const uint8_t* sz_src = wsrc;  // (scale, zero) segment of the group in progress
+      // the end of the work list is one sentinel stage per group
+      const int stages = done ? kGroups : nst;
+      for (int s = 0; s < stages && ok; ++s, ++t) {
+        const int slot = t % kSlots;
+        const uint32_t par = static_cast<uint32_t>(t / kSlots) & 1u;
+        const uint32_t full = smem_addr(&H.slot_full[slot]);
+        ok = warp_wait(smem_addr(&H.slot_empty[slot]), par ^ 1u, a, abort);
+        if (!ok) break;
+        if (lane == 0) {
+          H.slot_item[slot] = done ? -1 : item;
+          H.slot_stage[slot] = s;
+          H.slot_seq[slot] = seq;
+          if (done) {
+            issued_mask &= ~(1u << slot);  // this phase carries no copies
+            mbar_arrive(full);
+            ++sentinels;
+          } else {
+            const int ngrp = groups_in_stage(s, a.g);
+            const uint32_t seg = kCodeBytes + kSzBytes * ngrp;
+            const uint32_t dst = smem_addr(ring + slot * kSlotBytes);
+            if (ngrp > 0) {
+              mbar_arrive_expect_tx(full, seg + nbox * kBBoxRows * 128);
+              bulk_g2s(dst + kCodeOff - kSzBytes * ngrp, wsrc, seg, full);
+              sz_src = wsrc;
+            } else {
+              // a stage inside a group (groups of 128) gets a copy of the group's (scale, zero)
+              // pairs (from L2) so that every slot is self-contained
+              mbar_arrive_expect_tx(full, kSzBytes + seg + nbox * kBBoxRows * 128);
+              bulk_g2s(dst + kCodeOff - kSzBytes, sz_src, kSzBytes, full);
+              bulk_g2s(dst + kCodeOff, wsrc, seg, full);
+            }
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d(dst + b * kBBoxRows * 128, &bmap, s * kStageK, pos0 + b * kBBoxRows, full);
+            wsrc += seg;
+            issued_mask |= 1u << slot;
+            issued_par = (issued_par & ~(1u << slot)) | (par << slot);
+          }
+        }
+        sentinels = __shfl_sync(0xffffffffu, sentinels, 0);
+        __syncwarp();
+      }
+      ++seq;
+    }
+    // drain: every bulk copy this warp issued has landed before the CTA can exit
+    if (lane == 0)
+      for (int i = 0; i < kSlots; ++i)
+        if ((issued_mask >> i) & 1u) mbar_wait(smem_addr(&H.slot_full[i]), (issued_par >> i) & 1u, a.err);
+  } else if (warp <= kIssuers) {
+    // ------------------------------------------------------------------ MMA issuers
+    if (lane == 0) {
+      const int r = warp - 1;                              // issuer 0..1
+      const int k0 = 2 * r;                                // its two k16 steps of every stage
+      // descriptor of slot 0's activation tile; slot i adds i * kSlotBytes / 16, k16 step kk adds 2 * kk
+      const uint64_t desc0 = sw128_desc(smem_addr(ring)) + 2 * k0;
+      uint32_t idesc = f16_idesc(16);
+      bool ok = true;
+      int t = 0;
+      for (int seq = 0; ok; ++seq) {
+        const int b = seq & 1;
+        const uint32_t dcol = tmem + kDCol0 + b * kDCols + r * kNMax;
+        for (int s = 0; s < nst; ++s, ++t) {
+          const int ast = t % kAStages, slot = t % kSlots;
+          // the stage is in TMEM; the dequant warps read the slot header before arriving
+          ok = wait_or_abort(smem_addr(&H.a_full[ast]), static_cast<uint32_t>(t / kAStages) & 1u, a, abort);
+          if (!ok) break;
+          if (s == 0) {  // a new item (or the end of the work list)
+            const int item = H.slot_item[slot];
+            if (item < 0) {
+              ok = false;
+              break;
+            }
+            int e, blk, n_cnt, pos0;
+            decode_item(item, H.prefix, a, e, blk, n_cnt, pos0);
+            idesc = f16_idesc((n_cnt + 15) & ~15);
+            // the accumulators are free once the epilogue two items back has read them
+            ok = wait_or_abort(smem_addr(&H.d_free[b]), (static_cast<uint32_t>(seq >> 1) & 1u) ^ 1u, a, abort);
+            if (!ok) break;
+          }
+          tc_fence_after();
+          const uint64_t bdesc = desc0 + static_cast<uint64_t>(slot * (kSlotBytes >> 4));
+          const uint32_t acol = tmem + ast * kACols + 8 * k0;
+          tc_mma(dcol, acol, bdesc, idesc, s > 0 ? 1u : 0u);
+          tc_mma(dcol, acol + 8, bdesc + 2, idesc, 1u);
+          tc_commit(smem_addr(&H.slot_empty[slot]));  // slot and (for the group) TMEM stage reusable
+        }
+        if (ok) tc_commit(smem_addr(&H.d_full[b]));
+      }
+      // every MMA issued has completed before tensor memory is freed
+      tc_commit(smem_addr(&H.drain));
+      mbar_wait(smem_addr(&H.drain), 0, a.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ dequant groups
+    const int grp = (warp - kFirstDqWarp) >> 2;
+    const int q = warp & 3;              // TMEM lane quadrant (rows 32q .. 32q+31)
+    const int m = 32 * q + lane;         // GEMM row within the 128-row block
+    const uint32_t lane_bits = static_cast<uint32_t>(32 * q) << 16;
+    float* xch = xch_all + grp * 64 * kXchStride;
+    __half2 z0 = bits_h2(0u), z1 = bits_h2(0u), s0 = bits_h2(0u), s1 = bits_h2(0u);  // current group(s) of row m
+    int cur = -1, n_cnt = 0, pos0 = 0, blk = 0, e = 0;
+    uint32_t xphase = 0;
+    bool ok = true;
+    for (int t = grp; ok; t += kGroups) {
+      const int slot = t % kSlots;
+      ok = warp_wait(smem_addr(&H.slot_full[slot]), static_cast<uint32_t>(t / kSlots) & 1u, a, abort);
+      if (!ok) break;
+      const int item = H.slot_item[slot];
+      const int s = H.slot_stage[slot];
+      const int seq = H.slot_seq[slot];
+      if (item < 0) {  // end of the work list: pass it on to the issuers, which learn of stages via a_full
+        // (only after the stage that last used this TMEM stage was consumed, so a_full never runs a
+        // phase ahead)
+        if (t >= kAStages) {
+          const int tp = t - kAStages;
+          ok = warp_wait(smem_addr(&H.slot_empty[tp % kSlots]), static_cast<uint32_t>(tp / kSlots) & 1u, a, abort);
+          if (!ok) break;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&H.a_full[t % kAStages]));
+        break;
+      }
+      if (item != cur) {
+        decode_item(item, H.prefix, a, e, blk, n_cnt, pos0);
+        cur = item;
+      }
+      const uint8_t* st = ring + slot * kSlotBytes;
+      // (scale, zero) of row m for the group(s) of this stage (every slot carries them)
+      const int ngrp = max(groups_in_stage(s, a.g), 1);
+      const uint32_t* sz = reinterpret_cast<const uint32_t*>(st + kCodeOff - kSzBytes * ngrp);
+      {
+        const __half2 v0 = bits_h2(sz[m]);
+        const __half2 v1 = ngrp > 1 ? bits_h2(sz[kBlockRows + m]) : v0;
+        s0 = __low2half2(v0);
+        s1 = __low2half2(v1);
+        z0 = __high2half2(v0);
+        z1 = __high2half2(v1);
+      }
+      // this row's 64 codes: two 16-byte halves, [half][row][16 B]; with groups of 32
+      // the second half belongs to the stage's second group
+      const uint4 c0 = *reinterpret_cast<const uint4*>(st + kCodeOff + m * 16);
+      const uint4 c1 = *reinterpret_cast<const uint4*>(st + kCodeOff + kBlockRows * 16 + m * 16);
+      uint32_t w[32];
+      dequant_row8(c0.x, z0, s0, w + 0);
+      dequant_row8(c0.y, z0, s0, w + 4);
+      dequant_row8(c0.z, z0, s0, w + 8);
+      dequant_row8(c0.w, z0, s0, w + 12);
+      dequant_row8(c1.x, z1, s1, w + 16);
+      dequant_row8(c1.y, z1, s1, w + 20);
+      dequant_row8(c1.z, z1, s1, w + 24);
+      dequant_row8(c1.w, z1, s1, w + 28);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&H.slot_empty[slot]));  // codes and scales are in registers
+      const int ast = t % kAStages;
+      if (t >= kAStages) {
+        // the TMEM stage is free once the MMAs of the stage that used it last (t - kAStages)
+        // have completed: that stage's slot is released by the issuers' commits (and our arrivals)
+        const int tp = t - kAStages;
+        ok = warp_wait(smem_addr(&H.slot_empty[tp % kSlots]), static_cast<uint32_t>(tp / kSlots) & 1u, a, abort);
+        if (!ok) break;
+      }
+      tc_fence_after();
+      tc_st32(tmem + lane_bits + ast * kACols, w);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&H.a_full[ast]));
+      if (s == nst - 1) {
+        // ------------------------------------------------------------ accumulators
+        const int b = seq & 1;
+        ok = warp_wait(smem_addr(&H.d_full[b]), static_cast<uint32_t>(seq >> 1) & 1u, a, abort);
+        if (!ok) break;
+        tc_fence_after();
+        float acc[kNMax];
+        {
+          const uint32_t dcol = tmem + lane_bits + kDCol0 + b * kDCols;
+          // accumulator of k16 steps 0-1 plus that of steps 2-3, in this order
+#pragma unroll
+          for (int c = 0; c < kNMax; c += 16) {
+            uint32_t v0[16], v1[16];
+            tc_ld16(dcol + c, v0);
+            tc_ld16(dcol + kNMax + c, v1);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[c + i] = __uint_as_float(v0[i]) + __uint_as_float(v1[i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&H.d_free[b]));  // the item after next may accumulate here
+        // ------------------------------------------------------------ epilogue
+        if (kEpi == 0) {
+          // rows 0..63 gate j = 64*blk + m, rows 64..127 up j = 64*blk + m - 64; the up rows
+          // reach the gate rows' threads through this group's exchange area (bounded
+          // mbarriers, not a named barrier, so a timed-out warp cannot strand the others)
+          if (q >= 2) {
+            ok = warp_wait(smem_addr(&H.xch_done[grp]), xphase ^ 1u, a, abort);  // previous reads finished
+            if (!ok) break;
+            float4* dst = reinterpret_cast<float4*>(xch + (m - 64) * kXchStride);
+#pragma unroll
+            for (int i = 0; i < kNMax / 4; ++i)
+              dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&H.xch_ready[grp]));
+          } else {
+            ok = warp_wait(smem_addr(&H.xch_ready[grp]), xphase, a, abort);
+            if (!ok) break;
+            const float4* up4 = reinterpret_cast<const float4*>(xch + m * kXchStride);
+            const int j = 64 * blk + m;
+#pragma unroll
+            for (int i = 0; i < kNMax / 4; ++i) {
+              const float4 u = up4[i];
+              const float up[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const int n = 4 * i + c;
+                if (n < n_cnt)
+                  a.h_out[static_cast<size_t>(pos0 + n) * a.f + j] =
+                      __half_as_ushort(__float2half_rn(gelu(acc[n], a.act) * up[c]));
+              }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&H.xch_done[grp]));
+          }
+          xphase ^= 1u;
+        } else {
+          const int i_row = kBlockRows * blk + m;
+#pragma unroll
+          for (int n = 0; n < kNMax; ++n)
+            if (n < n_cnt) a.y_out[static_cast<size_t>(a.pair_list[pos0 + n]) * a.d + i_row] = acc[n];
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+// Token rows of every (token, expert) pair, copied in expert-sorted order:
+// xs[pos] = x[pair_list[pos] / k].  One warp per row, 16-byte accesses.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ pair_list, int P, int k, int d,
+                                                          uint16_t* __restrict__ xs) {
+  const int pos = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (pos >= P) return;
+  const int t = pair_list[pos] / k;
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
+  uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<size_t>(pos) * d);
+  for (int i = lane; i < d / 8; i += 32) dst[i] = src[i];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// 2-D tensor map over rows x cols fp16 (row-major), box 64 columns x 16 rows, 128B swizzle.
+bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {kStageK, kBBoxRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t init_gemm_kernels(int* blocks_per_sm) {
+  for (const void* fn : {reinterpret_cast<const void*>(expert_gemm_tc_kernel<0>),
+                         reinterpret_cast<const void*>(expert_gemm_tc_kernel<1>)}) {
+    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (err != cudaSuccess) return err;
+  }
+  // Two CTAs per SM: shared memory, registers (launch bounds) and tensor memory
+  // (2 x 256 of 512 columns) all allow exactly two.
+  *blocks_per_sm = kCtasPerSm;
+  return cudaSuccess;
+}
+
+cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, const int32_t* expert_offsets,
+                               const int32_t* pair_list, const uint8_t* w, uint16_t* h, float* y, WsHeader* hdr,
+                               int grid, cudaStream_t st) {
+  const int P = static_cast<int>(s.pairs());
+  TcArgs a{};
+  a.w = w;
+  a.offsets = expert_offsets;
+  a.pair_list = pair_list;
+  a.E = s.E;
+  a.f = s.f;
+  a.d = s.d;
+  a.act = s.act;
+  a.err = &hdr->error;
+  a.h_out = h;
+  a.y_out = y;
+  CUtensorMap bmap;
+  if (which == 0) {  // gate_up: rows 2f in f/64 blocks of 64 gate + 64 up rows, K = d
+    // the token rows are first copied in expert order into the (still unused) y region
+    uint16_t* xs = reinterpret_cast<uint16_t*>(y);
+    gather_rows_kernel<<<(P + 7) / 8, 256, 0, st>>>(x, pair_list, P, s.k, s.d, xs);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    if (!make_row_map(&bmap, xs, P, s.d)) return cudaErrorInvalidValue;
+    a.K = s.d;
+    a.g = s.g1;
+    a.nblocks = s.f / 64;
+    a.counter = &hdr->next_item[0];
+    a.counter_to_reset = &hdr->next_item[1];
+  } else {           // down: rows d in d/128 blocks, K = f
+    if (!make_row_map(&bmap, h, P, s.f)) return cudaErrorInvalidValue;
+    a.K = s.f;
+    a.g = s.g2;
+    a.nblocks = s.d / kBlockRows;
+    a.counter = &hdr->next_item[1];
+    a.counter_to_reset = &hdr->next_item[0];
+  }
+  a.block_bytes = int64_t(kBlockRows) * a.K / 2 + int64_t(kBlockRows) * (a.K / a.g) * 4;
+  a.expert_bytes = a.block_bytes * a.nblocks;
+  if (which == 0) expert_gemm_tc_kernel<0><<<grid, kThreads, kSmemBytes, st>>>(a, bmap);
+  else expert_gemm_tc_kernel<1><<<grid, kThreads, kSmemBytes, st>>>(a, bmap);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

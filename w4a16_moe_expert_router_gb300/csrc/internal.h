@@ -13,7 +13,7 @@ namespace moe {
 // Tiling of the grouped dequant GEMMs (gate_up and down share it).
 constexpr int kBlockRows = 128;   // GEMM rows per work item (gate_up: 64 gate + 64 up rows)
 constexpr int kStageK = 64;       // contraction columns per pipeline stage
-constexpr int kChunkN = 64;       // tokens (pairs) per work item
+constexpr int kChunkN = 32;       // tokens (pairs) per work item
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr int64_t kMaxPairs = int64_t(1) << 22;

@@ -10,16 +10,16 @@
 // expert, per block of 128 GEMM rows, per stage of 64 columns:
 //   [(scale, zero) pairs of the block's 128 rows for each group starting in
 //    this stage, 512 bytes per group][4096 bytes of codes]
-// GEMM row order inside a block: 8 tiles of 16 rows.  For gate_up (R = 2f) tile
-// m of block b holds gate rows 64b+8m .. +7 then up rows f+64b+8m .. +7; for down
-// (R = d) it holds rows 128b+16m .. +15.  The codes of a stage are ordered
-// [tile m][lane][k16 step], one 32-bit word each, a word holding the eight
-// codes lane (g = lane/4, t = lane%4) needs for one m16n8k16 A fragment:
-//   bits  0..3  (row g,   col 2t)    bits 16..19 (row g,   col 2t+1)
-//   bits  4..7  (row g+8, col 2t)    bits 20..23 (row g+8, col 2t+1)
-//   bits  8..11 (row g,   col 2t+8)  bits 24..27 (row g,   col 2t+9)
-//   bits 12..15 (row g+8, col 2t+8)  bits 28..31 (row g+8, col 2t+9)
-// (rows relative to the tile, columns relative to the k16 step).
+// GEMM row r of block b is, for gate_up (R = 2f), gate row 64b+r for r < 64 and
+// up row f+64b+r-64 for r >= 64 (so a block's tensor-memory lanes 0..63 hold
+// gate rows and 64..127 the matching up rows); for down (R = d) it is row
+// 128b+r.  The codes of a stage are ordered [half h][GEMM row r][4 words]:
+// half h covers the stage's columns 32h .. 32h+31, and word w of (h, r) holds the
+// 8 codes of row r at columns c0 = 32h + 8w + {0..7} (relative to the stage),
+// nibble i (bits 4i..4i+3) holding column c0 + {0, 2, 4, 6, 1, 3, 5, 7}[i], the
+// order in which the kernels' dequantiser produces the f16x2 column pairs
+// (c0, c0+1), (c0+2, c0+3), ... it writes to tensor memory.  Each thread of the
+// dequantiser reads its row's two 16-byte halves.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -52,8 +52,7 @@ bool proj_of(const moe_w4a16_shape* sh, int32_t which, Proj* p) {
 
 // Matrix row of GEMM row r (0..127) of block b.
 inline int64_t gemm_row(const Proj& p, int64_t b, int r) {
-  const int m = r >> 4, i = r & 15;
-  if (p.gate_up) return i < 8 ? 64 * b + 8 * m + i : p.f + 64 * b + 8 * m + (i - 8);
+  if (p.gate_up) return r < 64 ? 64 * b + r : p.f + 64 * b + (r - 64);
   return moe::kBlockRows * b + r;
 }
 
@@ -61,9 +60,8 @@ inline int groups_in_stage(int64_t s, int64_t g) {
   return g <= moe::kStageK ? int(moe::kStageK / g) : ((s * moe::kStageK) % g == 0 ? 1 : 0);
 }
 
-// Column offsets (within a k16 step) of nibble i of a word, and whether it is row g+8.
-constexpr int kNibCol[8] = {0, 0, 8, 8, 1, 1, 9, 9};
-constexpr int kNibHi[8] = {0, 1, 0, 1, 0, 1, 0, 1};
+// Column offset (within a word's 8 columns) of nibble i of the word.
+constexpr int kNibCol[8] = {0, 2, 4, 6, 1, 3, 5, 7};
 
 double half_value(uint16_t h) {
   const int e = (h >> 10) & 31, m = h & 1023;
@@ -100,17 +98,16 @@ moe_w4a16_status walk(const Proj& p, uint8_t* q, uint16_t* scale, uint16_t* zero
             out += 4;
           }
         }
-        for (int m = 0; m < 8; ++m) {
-          for (int lane = 0; lane < 32; ++lane) {
-            const int gg = lane >> 2, t = lane & 3;
-            for (int kk = 0; kk < 4; ++kk) {
-              const int64_t c0 = s * moe::kStageK + kk * 16 + 2 * t;
+        for (int hf = 0; hf < 2; ++hf) {
+          for (int r = 0; r < moe::kBlockRows; ++r) {
+            uint8_t* qrow = qe + rows[r] * rowb;
+            for (int w = 0; w < 4; ++w) {
+              const int64_t c0 = s * moe::kStageK + hf * 32 + w * 8;
               uint32_t word = 0;
               if (!kPack) std::memcpy(&word, out, 4);
               for (int i = 0; i < 8; ++i) {
-                const int64_t row = rows[16 * m + gg + 8 * kNibHi[i]];
                 const int64_t col = c0 + kNibCol[i];
-                uint8_t* byte = qe + row * rowb + (col >> 1);
+                uint8_t* byte = qrow + (col >> 1);
                 const int sh = (col & 1) ? 4 : 0;
                 if (kPack) {
                   word |= uint32_t((*byte >> sh) & 15u) << (4 * i);

@@ -52,13 +52,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but lets the hardware suspend the thread for up to
+// `suspend_ns` while the phase is incomplete, so a waiting warp does not spin on
+// issue slots that working warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kSuspendNs = 1000000;  // 1 ms; a completed phase wakes the thread earlier
+
 // Waits for the phase of parity `parity` to complete, at most limit_ns.  On
 // timeout records the status in *err and returns false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err,
                                           uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kSuspendNs)) {
     if (global_timer_ns() - t0 > limit_ns) {
       atomicExch(err, kStatusTimeout);
       return false;
