@@ -19,10 +19,12 @@
 // items = (expert, 128-row block, chunk of <= 32 tokens) taken from a global
 // counter, each item self-contained so results do not depend on which CTA ran
 // it; the CTA's stages are numbered t = 0, 1, ... across its items):
-//   warp 0      producer: per 64-column stage, one 1-D bulk copy of the block's
-//               stream segment (scale/zero pairs + codes) and 2-D TMA loads
-//               (128-byte swizzle, 16-row boxes) of the item's activation rows
-//               into a ring of eight shared-memory slots (mbarrier complete_tx);
+//   warp 0      producer: claims items one ahead of use; per 64-column stage it
+//               writes the decoded item (stage, tokens, block, first row) into
+//               the slot header and issues one 1-D bulk copy of the block's
+//               stream segment (scale/zero pairs + codes) and one 2-D TMA load
+//               (128-byte swizzle, 32 token rows) of the activations into a ring
+//               of eight shared-memory slots (mbarrier complete_tx);
 //   warps 1-2   MMA issuers (warp 1 also allocates tensor memory): one lane
 //               each; issuer i issues the tcgen05.mma of k16 steps 2i and 2i+1 of
 //               every stage into its own fp32 accumulator (A = dequantised
@@ -31,14 +33,15 @@
 //               occupies the issuing thread for ~50-90 cycles whatever N is, so
 //               two issuers share that cost; each commits once per stage
 //               (releasing the slot and the TMEM stage) and once per item;
-//   warps 3-6   dequantisers, one warp per TMEM lane quadrant: each thread owns
-//               one GEMM row and writes the row's 64 weights of a stage into one
-//               of four TMEM stages (one tcgen05.st of 32 columns); at an item's
-//               last stage the same warps read the row's two accumulators
-//               (tcgen05.ld, added in a fixed order) and run the epilogue -- the
-//               gated GELU through a shared-memory exchange of the up rows, or
-//               the fp32 row stores of the down projection -- while the issuers
-//               already fill the other accumulator set.
+//   warps 3-10  two dequant groups of four warps, one warp per TMEM lane
+//               quadrant; group G takes the stages t = G mod 2: each thread owns
+//               one GEMM row and writes the row's 64 weights of the stage into
+//               the stage's TMEM buffer (one tcgen05.st of 32 columns).  The
+//               group that gets an item's last stage reads the row's two
+//               accumulators (tcgen05.ld, added in a fixed order) and runs the
+//               epilogue -- the gated GELU through a shared-memory exchange of
+//               the up rows, or the fp32 row stores of the down projection --
+//               while the other group carries on with the next item.
 // Every wait is bounded: on expiry the CTA records MOE_W4A16_ERR_TIMEOUT in the
 // workspace and all roles leave their loops, drain what is in flight and free
 // tensor memory.  No split-K and no atomics on data.
@@ -54,7 +57,7 @@
 namespace moe {
 namespace {
 
-constexpr int kGroups = 1;                     // dequant groups (four warps each, one per lane quadrant)
+constexpr int kGroups = 2;                     // dequant groups (four warps each, one per lane quadrant)
 constexpr int kDqWarps = 4 * kGroups;
 constexpr int kIssuers = 2;                    // MMA issuers: k16 steps {0,1} and {2,3} of every stage
 constexpr int kFirstDqWarp = 1 + kIssuers;
@@ -71,7 +74,7 @@ constexpr int kTmemCols = 256;
 static_assert(kDCol0 + kDBufs * kDCols <= kTmemCols, "TMEM budget");
 static_assert(kNMax == 32, "the dequant warps hold 32 accumulator columns");
 static_assert(kSlots % kAStages == 0, "stage t uses slot t % kSlots and TMEM stage t % kAStages");
-constexpr int kBBoxRows = 16;                  // TMA box: 64 columns x 16 rows = 2 KiB
+constexpr int kBBoxRows = 32;                  // TMA box: 64 columns x 32 rows = 4 KiB
 constexpr int kBBytes = kNMax * 128;           // 4 KiB, 128B-swizzled K-major
 constexpr int kSzBytes = kBlockRows * 4;       // 512: (scale, zero) of 128 rows for one group
 constexpr int kCodeBytes = kBlockRows * kStageK / 2;  // 4096
@@ -80,7 +83,7 @@ constexpr int kSlotBytes = 10240;                     // multiple of 1024
 static_assert(kCodeOff + kCodeBytes <= kSlotBytes && kSlotBytes % 1024 == 0, "slot layout");
 constexpr int kXchStride = kNMax + 4;          // floats per exchanged row (bank-conflict padding)
 constexpr int kXchBytes = kGroups * 64 * kXchStride * 4;  // one exchange area per group
-constexpr int kHeaderBytes = 2048;
+constexpr int kHeaderBytes = 4096;
 constexpr int kRingOff = (kHeaderBytes + kXchBytes + 1023) / 1024 * 1024;
 constexpr int kSmemBytes = 1024 + kRingOff + kSlots * kSlotBytes;  // +1024 for alignment
 
@@ -112,12 +115,13 @@ struct __align__(8) TcHeader {
   uint64_t drain;
   uint64_t xch_ready[kGroups];  // the 2 up-row warps of a group have written their rows
   uint64_t xch_done[kGroups];   // the 2 gate-row warps of a group have read them
-  int slot_item[kSlots];
-  int slot_stage[kSlots];
+  int slot_desc[kSlots];        // stage | tokens << 8 | block << 16, or -1 at the end of the work list
+  int slot_pos0[kSlots];        // first expert-sorted row of the item's tokens
   int slot_seq[kSlots];         // the item's sequence number within this CTA
   uint32_t tmem_base;
   int abort;
   int prefix[kMaxExperts + 1];
+  int offs[kMaxExperts + 1];    // expert_offsets, copied once
 };
 static_assert(sizeof(TcHeader) <= kHeaderBytes, "header fits");
 
@@ -138,17 +142,17 @@ __device__ __forceinline__ int expert_of(int item, const int* prefix, int E) {
 
 // Work item -> (expert, 128-row block, token chunk); the chunk varies fastest,
 // so concurrent items of a busy expert share weight blocks in L2.
-__device__ __forceinline__ void decode_item(int item, const int* prefix, const TcArgs& a, int& expert, int& blk,
-                                            int& n_cnt, int& pos0) {
+__device__ __forceinline__ void decode_item(int item, const int* prefix, const int* offs, const TcArgs& a,
+                                            int& expert, int& blk, int& n_cnt, int& pos0) {
   const int e = expert_of(item, prefix, a.E);
-  const int n_e = a.offsets[e + 1] - a.offsets[e];
+  const int n_e = offs[e + 1] - offs[e];
   const int nch = (n_e + kChunkN - 1) / kChunkN;
   const int r = item - prefix[e];
   const int c = r % nch;
   expert = e;
   blk = r / nch;
   n_cnt = min(kChunkN, n_e - kChunkN * c);
-  pos0 = a.offsets[e] + kChunkN * c;
+  pos0 = offs[e] + kChunkN * c;
 }
 
 // --- tcgen05 wrappers ---------------------------------------------------------
@@ -328,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int j = 0; j < 8; ++j)
       if (lane * 8 + j < a.E) H.prefix[lane * 8 + j] = incl - sum + loc[j];
     if (lane == 31) H.prefix[a.E] = incl;
+    for (int e = lane; e <= a.E; e += 32) H.offs[e] = a.offsets[e];
   }
   tc_fence_before();
   __syncthreads();
@@ -343,13 +348,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint32_t issued_mask = 0;   // slots whose last phase carried copies
     uint32_t issued_par = 0;    // parity of that phase, one bit per slot
     bool ok = true;
+    // the next item is claimed one item ahead, so the atomic's latency hides behind this item's stages
+    int next = 0;
+    if (lane == 0) next = atomicAdd(a.counter, 1);
     while (ok && sentinels < kGroups) {
-      int item = 0;
-      if (lane == 0) item = atomicAdd(a.counter, 1);
-      item = __shfl_sync(0xffffffffu, item, 0);
+      const int item = __shfl_sync(0xffffffffu, next, 0);
       const bool done = item >= total;
+      if (lane == 0 && !done) next = atomicAdd(a.counter, 1);
       int e = 0, blk = 0, n_cnt = 0, pos0 = 0;
-      if (!done) decode_item(item, H.prefix, a, e, blk, n_cnt, pos0);
+      if (!done) decode_item(item, H.prefix, H.offs, a, e, blk, n_cnt, pos0);
       const int nbox = (n_cnt + kBBoxRows - 1) / kBBoxRows;
       const uint8_t* wsrc =
           a.w + static_cast<int64_t>(e) * a.expert_bytes + static_cast<int64_t>(blk) * a.block_bytes;
@@ -363,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         ok = warp_wait(smem_addr(&H.slot_empty[slot]), par ^ 1u, a, abort);
         if (!ok) break;
         if (lane == 0) {
-          H.slot_item[slot] = done ? -1 : item;
-          H.slot_stage[slot] = s;
+          H.slot_desc[slot] = done ? -1 : (s | (n_cnt << 8) | (blk << 16));
+          H.slot_pos0[slot] = pos0;
           H.slot_seq[slot] = seq;
           if (done) {
             issued_mask &= ~(1u << slot);  // this phase carries no copies
@@ -420,13 +427,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           ok = wait_or_abort(smem_addr(&H.a_full[ast]), static_cast<uint32_t>(t / kAStages) & 1u, a, abort);
           if (!ok) break;
           if (s == 0) {  // a new item (or the end of the work list)
-            const int item = H.slot_item[slot];
-            if (item < 0) {
+            const int desc = H.slot_desc[slot];
+            if (desc < 0) {
               ok = false;
               break;
             }
-            int e, blk, n_cnt, pos0;
-            decode_item(item, H.prefix, a, e, blk, n_cnt, pos0);
+            const int n_cnt = (desc >> 8) & 0xff;
             idesc = f16_idesc((n_cnt + 15) & ~15);
             // the accumulators are free once the epilogue two items back has read them
             ok = wait_or_abort(smem_addr(&H.d_free[b]), (static_cast<uint32_t>(seq >> 1) & 1u) ^ 1u, a, abort);
@@ -454,17 +460,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const uint32_t lane_bits = static_cast<uint32_t>(32 * q) << 16;
     float* xch = xch_all + grp * 64 * kXchStride;
     __half2 z0 = bits_h2(0u), z1 = bits_h2(0u), s0 = bits_h2(0u), s1 = bits_h2(0u);  // current group(s) of row m
-    int cur = -1, n_cnt = 0, pos0 = 0, blk = 0, e = 0;
+    int n_cnt = 0, pos0 = 0, blk = 0;
     uint32_t xphase = 0;
     bool ok = true;
     for (int t = grp; ok; t += kGroups) {
       const int slot = t % kSlots;
       ok = warp_wait(smem_addr(&H.slot_full[slot]), static_cast<uint32_t>(t / kSlots) & 1u, a, abort);
       if (!ok) break;
-      const int item = H.slot_item[slot];
-      const int s = H.slot_stage[slot];
+      const int desc = H.slot_desc[slot];
       const int seq = H.slot_seq[slot];
-      if (item < 0) {  // end of the work list: pass it on to the issuers, which learn of stages via a_full
+      if (desc < 0) {  // end of the work list: pass it on to the issuers, which learn of stages via a_full
         // (only after the stage that last used this TMEM stage was consumed, so a_full never runs a
         // phase ahead)
         if (t >= kAStages) {
@@ -476,10 +481,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (lane == 0) mbar_arrive(smem_addr(&H.a_full[t % kAStages]));
         break;
       }
-      if (item != cur) {
-        decode_item(item, H.prefix, a, e, blk, n_cnt, pos0);
-        cur = item;
-      }
+      const int s = desc & 0xff;
+      n_cnt = (desc >> 8) & 0xff;
+      blk = desc >> 16;
+      pos0 = H.slot_pos0[slot];
       const uint8_t* st = ring + slot * kSlotBytes;
       // (scale, zero) of row m for the group(s) of this stage (every slot carries them)
       const int ngrp = max(groups_in_stage(s, a.g), 1);

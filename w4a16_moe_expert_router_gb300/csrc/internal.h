@@ -22,7 +22,8 @@ constexpr int64_t kMaxPairs = int64_t(1) << 22;
 struct WsHeader {
   int32_t error;          // sticky moe_w4a16_status of device-side failures
   int32_t next_item[2];   // dynamic work counters of the gate_up (0) and down (1) kernels
-  int32_t pad[61];
+  uint32_t route_ticket;  // CTAs of the routing launch that have finished their top-k (reset by the last)
+  int32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -1,11 +1,17 @@
-// route.cu -- routing of a canvas: top-k experts per token, softmax over the
-// selected logits, and the per-expert pair lists.
+// route.cu -- routing of a canvas in one launch: top-k experts per token,
+// softmax over the selected logits, and the per-expert pair lists.
 //
 // Model card "srswti/axe-diffusion-ksl-xe", "what the model is": every token is
 // routed to its top-8 of 128 experts.  "The kernels we built": one launch then
 // serves all experts, so pairs are grouped by expert here; the grouping is a
 // stable counting sort (pair id ascending inside an expert) with no atomics on
 // positions, so the lists are identical from run to run.
+//
+// Every CTA ranks the experts of 32 tokens (one warp per token).  The CTA that
+// finishes last -- it learns so from a ticket counter in the workspace header,
+// taken after its top-k results are fenced -- then groups all pairs by expert.
+// No CTA waits for another, so the launch cannot stall however its CTAs are
+// scheduled.
 #include <cfloat>
 #include <climits>
 
@@ -15,9 +21,8 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteWarps = 8;    // tokens per CTA of the top-k kernel
-constexpr int kPermThreads = 1024;
-constexpr int kPermWarps = kPermThreads / 32;
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;  // tokens per CTA
 
 // Router order: larger logit first; equal logits (fp32 compare, so -0 == +0)
 // go to the lower expert index.  An id of INT_MAX marks "no candidate".
@@ -27,14 +32,10 @@ __device__ __forceinline__ bool ranks_before(float a, int ea, float b, int eb) {
   return a > b || (a == b && ea < eb);
 }
 
-// One warp per token.  Lane j holds logits of experts j, j+32, ... (E <= 256).
-__global__ void __launch_bounds__(kRouteWarps * 32) topk_softmax_kernel(const float* __restrict__ logits, int T,
-                                                                         int E, int k, int32_t* __restrict__ topk_idx,
-                                                                         float* __restrict__ topk_w) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* row = logits + static_cast<size_t>(t) * E;
+// Top-k of one token's E logits by one warp (lane j holds experts j, j+32, ...;
+// E <= 256), then the softmax over the k selected logits, summed in rank order.
+__device__ __forceinline__ void topk_softmax_warp(const float* __restrict__ row, int E, int k, int lane,
+                                                  int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
   float v[kMaxExperts / 32];
   uint32_t avail = 0;
 #pragma unroll
@@ -76,7 +77,6 @@ __global__ void __launch_bounds__(kRouteWarps * 32) topk_softmax_kernel(const fl
       sel_e[r] = be;
     }
   }
-  // softmax over the k selected logits, summed in rank order
   const float m = sel_v[0];
   float den = 0.f;
 #pragma unroll
@@ -85,37 +85,55 @@ __global__ void __launch_bounds__(kRouteWarps * 32) topk_softmax_kernel(const fl
 #pragma unroll
   for (int r = 0; r < kMaxTopK; ++r)
     if (r < k && r == lane) {
-      topk_idx[static_cast<size_t>(t) * k + r] = sel_e[r];
-      topk_w[static_cast<size_t>(t) * k + r] = expf(sel_v[r] - m) / den;
+      idx_out[r] = sel_e[r];
+      w_out[r] = expf(sel_v[r] - m) / den;
     }
 }
 
-// Single CTA: expert_offsets and pair_list from topk_idx.  Pairs are visited
-// in rounds of kPermThreads in pair order; a pair's slot is its expert's base
-// plus the number of earlier pairs (same round, lower warp or lower lane) with
-// the same expert, so the result is the stable order by construction.
-__global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __restrict__ topk_idx, int P, int E,
-                                                               int32_t* __restrict__ expert_offsets,
-                                                               int32_t* __restrict__ pair_list) {
-  __shared__ int cnt[kMaxExperts];
-  __shared__ int base[kMaxExperts];
-  __shared__ int wcnt[kPermWarps][kMaxExperts];
+// Stable grouping of the P pairs by expert, by one CTA of kRouteThreads.  Warp w
+// owns the contiguous pair range [w*chunk, (w+1)*chunk); pass 1 counts each
+// warp's pairs per expert, a scan over (expert, warp) turns the counts into
+// first positions, pass 2 places every pair at its warp's running position for
+// its expert.  Within a warp, pairs go in rounds of 32 in pair order and a pair's
+// rank among equal experts of its round is the number of lower lanes with the
+// same expert, so the order inside an expert is the pair order.
+__device__ __forceinline__ void group_pairs_block(const int32_t* __restrict__ topk_idx, int P, int E,
+                                                  int32_t* __restrict__ expert_offsets,
+                                                  int32_t* __restrict__ pair_list) {
+  __shared__ int cnt[kRouteWarps][kMaxExperts];  // per warp and expert: count, then next position
+  __shared__ int base[kMaxExperts + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < kMaxExperts; e += kPermThreads) cnt[e] = 0;
-  for (int i = tid; i < kPermWarps * kMaxExperts; i += kPermThreads) (&wcnt[0][0])[i] = 0;
+  for (int i = tid; i < kRouteWarps * kMaxExperts; i += kRouteThreads) (&cnt[0][0])[i] = 0;
   __syncthreads();
-  for (int p = tid; p < P; p += kPermThreads) {
-    const int e = topk_idx[p];
-    if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&cnt[e], 1);  // integer count
+  const int chunk = (P + kRouteWarps - 1) / kRouteWarps;
+  const int p_lo = warp * chunk, p_hi = min(P, p_lo + chunk);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int r0 = p_lo; r0 < p_hi; r0 += 32) {
+    const int p = r0 + lane;
+    int e = p < p_hi ? __ldcg(topk_idx + p) : -1;
+    if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && __popc(peers & lt_mask) == 0) cnt[warp][e] += __popc(peers);
+    __syncwarp();
   }
   __syncthreads();
-  if (warp == 0) {  // exclusive scan of cnt[0..E) : lane owns 8 consecutive experts
+  if (tid < E) {  // per expert: exclusive scan over the warps, total in tot
+    int run = 0;
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const int c = cnt[w][tid];
+      cnt[w][tid] = run;
+      run += c;
+    }
+    base[tid] = run;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the expert totals: lane owns 8 consecutive experts
     int local[8], sum = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int e = lane * 8 + j;
       local[j] = sum;
-      sum += (e < E) ? cnt[e] : 0;
+      sum += e < E ? base[e] : 0;
     }
     int incl = sum;
 #pragma unroll
@@ -124,6 +142,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
       if (lane >= off) incl += o;
     }
     const int excl = incl - sum;
+    __syncwarp();
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int e = lane * 8 + j;
@@ -135,43 +154,48 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(const int32_t* __
     if (lane == 31) expert_offsets[E] = incl;
   }
   __syncthreads();
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (int r0 = 0; r0 < P; r0 += kPermThreads) {
-    const int p = r0 + tid;
-    int e = (p < P) ? topk_idx[p] : -1;
+  for (int r0 = p_lo; r0 < p_hi; r0 += 32) {
+    const int p = r0 + lane;
+    int e = p < p_hi ? __ldcg(topk_idx + p) : -1;
     if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) e = -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lt_mask);
-    if (e >= 0 && rank == 0) wcnt[warp][e] = __popc(peers);
-    __syncthreads();
-    if (e >= 0) {
-      int before = 0;
-      for (int w = 0; w < warp; ++w) before += wcnt[w][e];
-      pair_list[base[e] + before + rank] = p;
-    }
-    __syncthreads();
-    for (int ee = tid; ee < E; ee += kPermThreads) {
-      int tot = 0;
-      for (int w = 0; w < kPermWarps; ++w) {
-        tot += wcnt[w][ee];
-        wcnt[w][ee] = 0;
-      }
-      base[ee] += tot;
-    }
-    __syncthreads();
+    if (e >= 0) pair_list[base[e] + cnt[warp][e] + rank] = p;
+    __syncwarp();
+    if (e >= 0 && rank == 0) cnt[warp][e] += __popc(peers);
+    __syncwarp();
   }
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                              int32_t* __restrict__ topk_idx,
+                                                              float* __restrict__ topk_w,
+                                                              int32_t* __restrict__ expert_offsets,
+                                                              int32_t* __restrict__ pair_list,
+                                                              uint32_t* __restrict__ ticket) {
+  __shared__ int is_last;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
+  if (t < T)
+    topk_softmax_warp(logits + static_cast<size_t>(t) * E, E, k, lane, topk_idx + static_cast<size_t>(t) * k,
+                      topk_w + static_cast<size_t>(t) * k);
+  __threadfence();  // this CTA's results are visible device-wide before its ticket is taken
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  group_pairs_block(topk_idx, T * k, E, expert_offsets, pair_list);
+  if (threadIdx.x == 0) *ticket = 0;  // ready for the next launch on this workspace
 }
 
 }  // namespace
 
 cudaError_t launch_route(const Dims& s, const float* logits, int32_t* topk_idx, float* topk_w,
-                         int32_t* expert_offsets, int32_t* pair_list, WsHeader* /*hdr*/, cudaStream_t st) {
+                         int32_t* expert_offsets, int32_t* pair_list, WsHeader* hdr, cudaStream_t st) {
   const int grid = (s.T + kRouteWarps - 1) / kRouteWarps;
-  topk_softmax_kernel<<<grid, kRouteWarps * 32, 0, st>>>(logits, s.T, s.E, s.k, topk_idx, topk_w);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  permute_kernel<<<1, kPermThreads, 0, st>>>(topk_idx, static_cast<int>(s.pairs()), s.E, expert_offsets,
-                                             pair_list);
+  route_kernel<<<grid, kRouteThreads, 0, st>>>(logits, s.T, s.E, s.k, topk_idx, topk_w, expert_offsets, pair_list,
+                                               &hdr->route_ticket);
   return cudaGetLastError();
 }
 
