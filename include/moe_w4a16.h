@@ -108,8 +108,9 @@ typedef struct {
 
 /* Bytes of device workspace that moe_w4a16_route and moe_w4a16_forward need for
  * this shape (0 on an invalid shape).  The workspace holds the intermediate
- * activations h (fp16 [T*k][f]) and per-pair expert outputs (fp32 [T*k][d]) plus
- * a small header (error word, work counters).  It must be initialised once with
+ * activations h (fp16 [T*k][f]), the token rows copied in expert order
+ * (fp16 [T*k][d]) and per-pair expert outputs (fp32 [T*k][d]) plus a small
+ * header (error word, work counters).  It must be initialised once with
  * moe_w4a16_workspace_init before its first use; later calls leave it ready. */
 MOE_W4A16_API size_t moe_w4a16_workspace_bytes(const moe_w4a16_shape* shape);
 
@@ -137,9 +138,20 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_forward(const moe_w4a16_shape* shape, c
                                    const moe_w4a16_weights* weights, const float* norm_gamma, float norm_eps,
                                    uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
 
-/* The three launches of moe_w4a16_forward, callable one by one on the same
- * stream in this order (same arguments and rules as moe_w4a16_forward; e.g. to
- * time each step or to interleave other work):
+/* The expert FFNs of moe_w4a16_forward without the combine: the gate_up and
+ * down GEMMs of every (token, expert) pair in one persistent launch, in which a
+ * down work item starts as soon as its expert's gate_up items have written
+ * their h rows ([MC] "the kernels we built": one launch for all experts).
+ * Leaves h and the per-pair rows y in the workspace for moe_w4a16_combine.
+ * Same arguments and rules as moe_w4a16_forward. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_experts(const moe_w4a16_shape* shape, const uint16_t* x,
+                                                 const moe_w4a16_routing* routing, const moe_w4a16_weights* weights,
+                                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* The steps of moe_w4a16_forward, callable one by one on the same stream in
+ * this order (same arguments and rules as moe_w4a16_forward; e.g. to time each
+ * step or to interleave other work); gate_up followed by down computes what
+ * moe_w4a16_experts computes, in two launches:
  *   moe_w4a16_gate_up  expert gate_up GEMMs with the gated GELU folded into the
  *                      epilogue: h = gelu(Wg x) * (Wu x) for every (token, expert)
  *                      pair -> fp16 rows in the workspace, ordered by expert
@@ -213,11 +225,11 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_unprepare(const moe_w4a16_shape* shape,
  * not call cudaMalloc because an allocation can synchronise the device and
  * stall the work already queued on it.
  *
- *   - The array holds MOE_W4A16_NOALLOC_SCRATCH_BYTES (24 MiB) and is reserved
+ *   - The array holds MOE_W4A16_NOALLOC_SCRATCH_BYTES (40 MiB) and is reserved
  *     on every GPU that loads the library until the process exits.
  *   - A shape whose moe_w4a16_workspace_bytes() exceeds that size is rejected
  *     with MOE_W4A16_ERR_WORKSPACE before anything is launched (a 256-token
- *     canvas with d = 2048, f = 704 and top-8 needs about 20 MB and fits; a
+ *     canvas with d = 2048, f = 704 and top-8 needs about 28 MB and fits; a
  *     1024-token batch of that layer does not).
  *   - The first call on a device performs a one-time set-up on that device (it
  *     looks up the array's device address and sets kernel attributes); make
@@ -230,7 +242,7 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_unprepare(const moe_w4a16_shape* shape,
  *   - A device-side wait that runs out is not reported (the error word sits in
  *     the static array); such a call's output is invalid.
  * Arguments are those of moe_w4a16_forward, without the workspace. */
-#define MOE_W4A16_NOALLOC_SCRATCH_BYTES ((size_t)24 << 20)
+#define MOE_W4A16_NOALLOC_SCRATCH_BYTES ((size_t)40 << 20)
 MOE_W4A16_API moe_w4a16_status moe_w4a16_forward_noalloc(const moe_w4a16_shape* shape, const uint16_t* x,
                                                          const moe_w4a16_routing* routing,
                                                          const moe_w4a16_weights* weights, const float* norm_gamma,

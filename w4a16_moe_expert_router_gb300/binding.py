@@ -23,10 +23,11 @@ OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE, ERR_TIM
 GATE_UP, DOWN = 0, 1
 
 EXPORTED = ("moe_w4a16_workspace_bytes", "moe_w4a16_workspace_init", "moe_w4a16_route", "moe_w4a16_forward",
+            "moe_w4a16_experts",
             "moe_w4a16_gate_up", "moe_w4a16_down", "moe_w4a16_combine", "moe_w4a16_read_error", "moe_w4a16_pack", "moe_w4a16_unpack", "moe_w4a16_prepared_bytes",
             "moe_w4a16_prepare", "moe_w4a16_unprepare", "moe_w4a16_status_string", "moe_w4a16_forward_noalloc")
 
-NOALLOC_SCRATCH_BYTES = 24 << 20  # MOE_W4A16_NOALLOC_SCRATCH_BYTES
+NOALLOC_SCRATCH_BYTES = 40 << 20  # MOE_W4A16_NOALLOC_SCRATCH_BYTES
 
 
 class MoeW4A16Error(RuntimeError):
@@ -73,6 +74,8 @@ def lib() -> ctypes.CDLL:
             L.moe_w4a16_forward.argtypes = [P(Shape), vp, P(Routing), P(Weights), vp, ctypes.c_float, vp, vp, sz, vp]
             L.moe_w4a16_forward.restype = st
             L.moe_w4a16_gate_up.argtypes = [P(Shape), vp, P(Routing), P(Weights), vp, sz, vp]
+            L.moe_w4a16_experts.restype = st
+            L.moe_w4a16_experts.argtypes = [P(Shape), vp, P(Routing), P(Weights), vp, sz, vp]
             L.moe_w4a16_gate_up.restype = st
             L.moe_w4a16_down.argtypes = [P(Shape), P(Routing), P(Weights), vp, sz, vp]
             L.moe_w4a16_down.restype = st
@@ -186,6 +189,13 @@ def moe_w4a16_forward_noalloc(shape: Shape, x, routing: RoutingBuffers, gate_up,
     _check(lib().moe_w4a16_forward_noalloc(ctypes.byref(shape), _dptr(x), ctypes.byref(r), ctypes.byref(w),
                                            _dptr(norm_gamma), float(norm_eps), _dptr(out), _stream(stream)),
            "moe_w4a16_forward_noalloc")
+
+
+def moe_w4a16_experts(shape: Shape, x, routing: RoutingBuffers, gate_up, down, workspace, stream=None) -> None:
+    r = routing.c()
+    w = Weights(_dptr(gate_up), _dptr(down))
+    _check(lib().moe_w4a16_experts(ctypes.byref(shape), _dptr(x), ctypes.byref(r), ctypes.byref(w), _dptr(workspace),
+                                   _nbytes(workspace), _stream(stream)), "moe_w4a16_experts")
 
 
 def moe_w4a16_gate_up(shape: Shape, x, routing: RoutingBuffers, gate_up, down, workspace, stream=None) -> None:

@@ -151,19 +151,16 @@ moe_w4a16_status run_forward_steps(const moe_w4a16_shape* shape, int steps, cons
   if ((steps & kCombine) && !(a.eps >= 0.f)) return MOE_W4A16_ERR_VALUE;
   const DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != MOE_W4A16_OK) return st;
-  auto* hdr = static_cast<moe::WsHeader*>(a.ws);
-  auto* base = static_cast<uint8_t*>(a.ws);
-  auto* h = reinterpret_cast<uint16_t*>(base + moe::ws_h_offset());
-  auto* y = reinterpret_cast<float*>(base + moe::ws_y_offset(s));
+  const moe::GemmWorkspace ws = moe::carve_workspace(a.ws, s);
   const auto cs = static_cast<cudaStream_t>(a.stream);
   const int grid = dev->num_sms * dev->gemm_blocks_per_sm;
-  if ((steps & kGateUp) && moe::launch_expert_gemm(0, s, a.x, r.expert_offsets, r.pair_list, a.weights->gate_up,
-                                                     h, y, hdr, grid, cs) != cudaSuccess)
+  // gate_up and down together run as one launch (down items wait for their expert's h rows)
+  const int gemm = ((steps & kGateUp) ? moe::kGemmGateUp : 0) | ((steps & kDown) ? moe::kGemmDown : 0);
+  if (gemm && moe::launch_expert_gemm(gemm, s, a.x, r.expert_offsets, r.pair_list,
+                                      (steps & kGateUp) ? a.weights->gate_up : nullptr,
+                                      (steps & kDown) ? a.weights->down : nullptr, ws, grid, cs) != cudaSuccess)
     return MOE_W4A16_ERR_CUDA;
-  if ((steps & kDown) && moe::launch_expert_gemm(1, s, nullptr, r.expert_offsets, r.pair_list, a.weights->down, h,
-                                                   y, hdr, grid, cs) != cudaSuccess)
-    return MOE_W4A16_ERR_CUDA;
-  if ((steps & kCombine) && moe::launch_combine(s, r.topk_w, y, a.gamma, a.eps, a.out, cs) != cudaSuccess)
+  if ((steps & kCombine) && moe::launch_combine(s, r.topk_w, ws.y, a.gamma, a.eps, a.out, cs) != cudaSuccess)
     return MOE_W4A16_ERR_CUDA;
   return MOE_W4A16_OK;
 }
@@ -177,6 +174,13 @@ moe_w4a16_status moe_w4a16_forward(const moe_w4a16_shape* shape, const uint16_t*
                                    uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
   return run_forward_steps(shape, kGateUp | kDown | kCombine,
                            FwdArgs{x, routing, weights, norm_gamma, norm_eps, out, workspace, workspace_bytes, stream});
+}
+
+moe_w4a16_status moe_w4a16_experts(const moe_w4a16_shape* shape, const uint16_t* x, const moe_w4a16_routing* routing,
+                                   const moe_w4a16_weights* weights, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  return run_forward_steps(shape, kGateUp | kDown,
+                           FwdArgs{x, routing, weights, nullptr, 0.f, nullptr, workspace, workspace_bytes, stream});
 }
 
 moe_w4a16_status moe_w4a16_gate_up(const moe_w4a16_shape* shape, const uint16_t* x, const moe_w4a16_routing* routing,

@@ -92,16 +92,11 @@ extern "C" moe_w4a16_status moe_w4a16_forward_noalloc(const moe_w4a16_shape* sha
   moe_w4a16_status st = device_setup(&dev);
   if (st != MOE_W4A16_OK) return st;
   const auto cs = static_cast<cudaStream_t>(stream);
-  auto* hdr = reinterpret_cast<moe::WsHeader*>(dev->scratch);
-  auto* h = reinterpret_cast<uint16_t*>(dev->scratch + moe::ws_h_offset());
-  auto* y = reinterpret_cast<float*>(dev->scratch + moe::ws_y_offset(s));
-  if (cudaMemsetAsync(hdr, 0, sizeof(moe::WsHeader), cs) != cudaSuccess) return MOE_W4A16_ERR_CUDA;
-  if (moe::launch_expert_gemm(0, s, x, r.expert_offsets, r.pair_list, weights->gate_up, h, y, hdr, dev->grid, cs) !=
-      cudaSuccess)
+  const moe::GemmWorkspace ws = moe::carve_workspace(dev->scratch, s);
+  if (cudaMemsetAsync(ws.hdr, 0, sizeof(moe::WsHeader), cs) != cudaSuccess) return MOE_W4A16_ERR_CUDA;
+  if (moe::launch_expert_gemm(moe::kGemmGateUp | moe::kGemmDown, s, x, r.expert_offsets, r.pair_list,
+                              weights->gate_up, weights->down, ws, dev->grid, cs) != cudaSuccess)
     return MOE_W4A16_ERR_CUDA;
-  if (moe::launch_expert_gemm(1, s, nullptr, r.expert_offsets, r.pair_list, weights->down, h, y, hdr, dev->grid,
-                              cs) != cudaSuccess)
-    return MOE_W4A16_ERR_CUDA;
-  if (moe::launch_combine(s, r.topk_w, y, norm_gamma, norm_eps, out, cs) != cudaSuccess) return MOE_W4A16_ERR_CUDA;
+  if (moe::launch_combine(s, r.topk_w, ws.y, norm_gamma, norm_eps, out, cs) != cudaSuccess) return MOE_W4A16_ERR_CUDA;
   return MOE_W4A16_OK;
 }

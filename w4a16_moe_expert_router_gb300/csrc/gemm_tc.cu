@@ -4,10 +4,15 @@
 // Model card "srswti/axe-diffusion-ksl-xe", "the kernels we built": the GEMM
 // reads packed nibbles and dequantises inline, so HBM carries real 4-bit
 // traffic; one launch covers all experts; the activation is folded into the
-// first GEMM's epilogue.  Two launches of one kernel template do the work:
+// first GEMM's epilogue.  One persistent launch runs both projections:
 //   gate_up:  a[p][n] = sum_k Wgu[e][n][k] x[t(p)][k]  (64 gate + 64 up rows per item)
 //             h[pos(p)][j] = gelu(a[p][j]) * a[p][f+j]  -> fp16, rows in expert-sorted order
 //   down:     y[p][i] = sum_j Wd[e][i][j] h[pos(p)][j]   -> fp32, rows by pair id p = t*k + r
+// The work list holds every gate_up item followed by every down item.  A down
+// item of expert e starts once all gate_up items of e have written their h rows
+// (a per-expert counter, bounded wait), so CTAs that run out of gate_up work go
+// straight on with down work instead of idling until the slowest CTA finishes.
+// The same kernel also runs one projection alone (the separate C entry points).
 //
 // Arithmetic: each weight is formed as w = fp16(fp16(q - z) * s): the offset
 // removal and q - z are exact in fp16 (unless |q - z| >= 8 needs a 12th
@@ -20,8 +25,8 @@
 // counter, each item self-contained so results do not depend on which CTA ran
 // it; the CTA's stages are numbered t = 0, 1, ... across its items):
 //   warp 0      producer: claims items one ahead of use; per 64-column stage it
-//               writes the decoded item (stage, tokens, block, first row) into
-//               the slot header and issues one 1-D bulk copy of the block's
+//               writes the decoded item (projection, stage, tokens, block, first
+//               row, expert) into the slot header and issues one 1-D bulk copy of the block's
 //               stream segment (scale/zero pairs + codes) and one 2-D TMA load
 //               (128-byte swizzle, 32 token rows) of the activations into a ring
 //               of eight shared-memory slots (mbarrier complete_tx);
@@ -87,22 +92,28 @@ constexpr int kHeaderBytes = 4096;
 constexpr int kRingOff = (kHeaderBytes + kXchBytes + 1023) / 1024 * 1024;
 constexpr int kSmemBytes = 1024 + kRingOff + kSlots * kSlotBytes;  // +1024 for alignment
 
-struct TcArgs {
+struct Proj {
   const uint8_t* w;         // prepared stream of the projection, all experts
   int64_t expert_bytes;     // stream bytes per expert
   int64_t block_bytes;      // stream bytes per 128-row block
   int nblocks;              // blocks per expert
   int K;                    // contraction length (multiple of 64)
   int g;                    // quantisation group along K (32, 64 or 128)
+};
+
+struct TcArgs {
+  Proj p[2];                // 0: gate_up, 1: down
+  int first, last;          // projections in this launch's work list (0 <= first <= last <= 1)
   const int32_t* offsets;   // [E+1]
   const int32_t* pair_list; // [T*k]
   int E;
-  uint16_t* h_out;          // gate_up output [T*k][f]
+  uint16_t* h;              // gate_up output, down input [T*k][f] (expert-sorted rows)
   float* y_out;             // down output [T*k][d]
   int f, d, act;
   int32_t* err;
-  int32_t* counter;
-  int32_t* counter_to_reset;
+  int32_t* counter;         // work counter of this launch
+  int32_t* done_ctas;       // CTAs that have finished; the last one resets both counters
+  int32_t* gu_done;         // [E] gate_up epilogues finished per expert (two per item)
 };
 
 // Shared-memory header (at the 1024-aligned base of dynamic shared memory).
@@ -115,12 +126,12 @@ struct __align__(8) TcHeader {
   uint64_t drain;
   uint64_t xch_ready[kGroups];  // the 2 up-row warps of a group have written their rows
   uint64_t xch_done[kGroups];   // the 2 gate-row warps of a group have read them
-  int slot_desc[kSlots];        // stage | tokens << 8 | block << 16, or -1 at the end of the work list
-  int slot_pos0[kSlots];        // first expert-sorted row of the item's tokens
+  int slot_desc[kSlots];        // stage | tokens << 8 | block << 16 | proj << 24 | last << 25, or -1 at the end
+  int slot_pos0[kSlots];        // first expert-sorted row of the item's tokens | expert << 22
   int slot_seq[kSlots];         // the item's sequence number within this CTA
   uint32_t tmem_base;
   int abort;
-  int prefix[kMaxExperts + 1];
+  int prefix[2][kMaxExperts + 1];  // items of each projection before expert e
   int offs[kMaxExperts + 1];    // expert_offsets, copied once
 };
 static_assert(sizeof(TcHeader) <= kHeaderBytes, "header fits");
@@ -140,11 +151,11 @@ __device__ __forceinline__ int expert_of(int item, const int* prefix, int E) {
   return lo;
 }
 
-// Work item -> (expert, 128-row block, token chunk); the chunk varies fastest,
-// so concurrent items of a busy expert share weight blocks in L2.
-__device__ __forceinline__ void decode_item(int item, const int* prefix, const int* offs, const TcArgs& a,
-                                            int& expert, int& blk, int& n_cnt, int& pos0) {
-  const int e = expert_of(item, prefix, a.E);
+// Work item of one projection -> (expert, 128-row block, token chunk); the chunk
+// varies fastest, so concurrent items of a busy expert share weight blocks in L2.
+__device__ __forceinline__ void decode_item(int item, const int* prefix, const int* offs, int E, int& expert,
+                                            int& blk, int& n_cnt, int& pos0) {
+  const int e = expert_of(item, prefix, E);
   const int n_e = offs[e + 1] - offs[e];
   const int nch = (n_e + kChunkN - 1) / kChunkN;
   const int r = item - prefix[e];
@@ -154,6 +165,8 @@ __device__ __forceinline__ void decode_item(int item, const int* prefix, const i
   n_cnt = min(kChunkN, n_e - kChunkN * c);
   pos0 = offs[e] + kChunkN * c;
 }
+
+constexpr uint64_t kDepWaitNs = 2000000000ull;  // bound of the wait for an expert's gate_up outputs
 
 // --- tcgen05 wrappers ---------------------------------------------------------
 
@@ -182,15 +195,6 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&v)[32])
       "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
       "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 
@@ -279,9 +283,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const T
   }
 }
 
-template <int kEpi>  // 0: gate_up with GeGLU epilogue, 1: down projection
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
-    expert_gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap bmap) {
+    expert_gemm_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap map_x,
+                          const __grid_constant__ CUtensorMap map_h) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TcHeader& H = *reinterpret_cast<TcHeader*>(smem);
@@ -290,7 +294,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   volatile int* abort = &H.abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (blockIdx.x == 0 && tid == 0) *a.counter_to_reset = 0;
   if (tid == 0) {
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(smem_addr(&H.slot_full[i]), 1);
@@ -314,36 +317,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  if (warp == 2) {  // items per expert = blocks * ceil(n_e / 32); exclusive scan, 8 experts per lane
-    int loc[8], sum = 0;
+  if (warp == 2) {  // items per expert = blocks * ceil(n_e / 32); exclusive scans, 8 experts per lane
+    for (int pj = 0; pj < 2; ++pj) {
+      const int nb = a.p[pj].nblocks;
+      int loc[8], sum = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = lane * 8 + j;
-      loc[j] = sum;
-      if (e < a.E) sum += a.nblocks * ((a.offsets[e + 1] - a.offsets[e] + kChunkN - 1) / kChunkN);
+      for (int j = 0; j < 8; ++j) {
+        const int e = lane * 8 + j;
+        loc[j] = sum;
+        if (e < a.E) sum += nb * ((a.offsets[e + 1] - a.offsets[e] + kChunkN - 1) / kChunkN);
+      }
+      int incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (lane * 8 + j < a.E) H.prefix[pj][lane * 8 + j] = incl - sum + loc[j];
+      if (lane == 31) H.prefix[pj][a.E] = incl;
     }
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (lane * 8 + j < a.E) H.prefix[lane * 8 + j] = incl - sum + loc[j];
-    if (lane == 31) H.prefix[a.E] = incl;
     for (int e = lane; e <= a.E; e += 32) H.offs[e] = a.offsets[e];
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = H.tmem_base;
-  const int total = H.prefix[a.E];
-  const int nst = a.K / kStageK;
+  // the launch's work list: [gate_up items][down items], restricted to projections first..last
+  const int total0 = a.first == 0 ? H.prefix[0][a.E] : 0;
+  const int total = total0 + (a.last == 1 ? H.prefix[1][a.E] : 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
-    if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&bmap) : "memory");
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&map_x) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&map_h) : "memory");
+    }
     int t = 0, seq = 0, sentinels = 0;
     uint32_t issued_mask = 0;   // slots whose last phase carried copies
     uint32_t issued_par = 0;    // parity of that phase, one bit per slot
@@ -355,11 +365,36 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int item = __shfl_sync(0xffffffffu, next, 0);
       const bool done = item >= total;
       if (lane == 0 && !done) next = atomicAdd(a.counter, 1);
+      const int pj = (a.first == 0 && item < total0) ? 0 : 1;
+      const Proj& P = a.p[pj];
       int e = 0, blk = 0, n_cnt = 0, pos0 = 0;
-      if (!done) decode_item(item, H.prefix, H.offs, a, e, blk, n_cnt, pos0);
-      const int nbox = (n_cnt + kBBoxRows - 1) / kBBoxRows;
+      if (!done) decode_item(pj == 0 ? item : item - total0, H.prefix[pj], H.offs, a.E, e, blk, n_cnt, pos0);
+      const int nst = P.K / kStageK;
+      if (!done && pj == 1 && a.first == 0 && lane == 0) {
+        // a down item reads the h rows of its expert: wait until every gate_up item of the
+        // expert has written them (two epilogue warps per item report)
+        const int need = 2 * a.p[0].nblocks * ((H.offs[e + 1] - H.offs[e] + kChunkN - 1) / kChunkN);
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+          int v;
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.gu_done + e) : "memory");
+          if (v >= need) break;
+          if (*abort || global_timer_ns() - t0 > kDepWaitNs) {
+            atomicExch(a.err, kStatusTimeout);
+            *abort = 1;
+            ok = false;
+            break;
+          }
+          __nanosleep(256);
+        }
+        // the TMA loads below read those rows through the async proxy
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      const CUtensorMap* bmap = pj == 0 ? &map_x : &map_h;
       const uint8_t* wsrc =
-          a.w + static_cast<int64_t>(e) * a.expert_bytes + static_cast<int64_t>(blk) * a.block_bytes;
+          P.w + static_cast<int64_t>(e) * P.expert_bytes + static_cast<int64_t>(blk) * P.block_bytes;
       const uint8_t* sz_src = wsrc;  // (scale, zero) segment of the group in progress
       // the end of the work list is one sentinel stage per group
       const int stages = done ? kGroups : nst;
@@ -370,30 +405,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         ok = warp_wait(smem_addr(&H.slot_empty[slot]), par ^ 1u, a, abort);
         if (!ok) break;
         if (lane == 0) {
-          H.slot_desc[slot] = done ? -1 : (s | (n_cnt << 8) | (blk << 16));
-          H.slot_pos0[slot] = pos0;
+          H.slot_desc[slot] =
+              done ? -1 : (s | (n_cnt << 8) | (blk << 16) | (pj << 24) | ((s == nst - 1 ? 1 : 0) << 25));
+          H.slot_pos0[slot] = pos0 | (e << 22);
           H.slot_seq[slot] = seq;
           if (done) {
             issued_mask &= ~(1u << slot);  // this phase carries no copies
             mbar_arrive(full);
             ++sentinels;
           } else {
-            const int ngrp = groups_in_stage(s, a.g);
+            const int ngrp = groups_in_stage(s, P.g);
             const uint32_t seg = kCodeBytes + kSzBytes * ngrp;
             const uint32_t dst = smem_addr(ring + slot * kSlotBytes);
             if (ngrp > 0) {
-              mbar_arrive_expect_tx(full, seg + nbox * kBBoxRows * 128);
+              mbar_arrive_expect_tx(full, seg + kBBoxRows * 128);
               bulk_g2s(dst + kCodeOff - kSzBytes * ngrp, wsrc, seg, full);
               sz_src = wsrc;
             } else {
               // a stage inside a group (groups of 128) gets a copy of the group's (scale, zero)
               // pairs (from L2) so that every slot is self-contained
-              mbar_arrive_expect_tx(full, kSzBytes + seg + nbox * kBBoxRows * 128);
+              mbar_arrive_expect_tx(full, kSzBytes + seg + kBBoxRows * 128);
               bulk_g2s(dst + kCodeOff - kSzBytes, sz_src, kSzBytes, full);
               bulk_g2s(dst + kCodeOff, wsrc, seg, full);
             }
-            for (int b = 0; b < nbox; ++b)
-              tma_load_2d(dst + b * kBBoxRows * 128, &bmap, s * kStageK, pos0 + b * kBBoxRows, full);
+            tma_load_2d(dst, bmap, s * kStageK, pos0, full);
             wsrc += seg;
             issued_mask |= 1u << slot;
             issued_par = (issued_par & ~(1u << slot)) | (par << slot);
@@ -418,24 +453,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       uint32_t idesc = f16_idesc(16);
       bool ok = true;
       int t = 0;
-      for (int seq = 0; ok; ++seq) {
-        const int b = seq & 1;
-        const uint32_t dcol = tmem + kDCol0 + b * kDCols + r * kNMax;
-        for (int s = 0; s < nst; ++s, ++t) {
-          const int ast = t % kAStages, slot = t % kSlots;
-          // the stage is in TMEM; the dequant warps read the slot header before arriving
+      while (ok) {
+        // first stage of an item (or the end of the work list): its header gives the item
+        {
+          const int ast = t % kAStages;
           ok = wait_or_abort(smem_addr(&H.a_full[ast]), static_cast<uint32_t>(t / kAStages) & 1u, a, abort);
           if (!ok) break;
-          if (s == 0) {  // a new item (or the end of the work list)
-            const int desc = H.slot_desc[slot];
-            if (desc < 0) {
-              ok = false;
-              break;
-            }
-            const int n_cnt = (desc >> 8) & 0xff;
-            idesc = f16_idesc((n_cnt + 15) & ~15);
-            // the accumulators are free once the epilogue two items back has read them
-            ok = wait_or_abort(smem_addr(&H.d_free[b]), (static_cast<uint32_t>(seq >> 1) & 1u) ^ 1u, a, abort);
+        }
+        const int desc = H.slot_desc[t % kSlots];
+        if (desc < 0) break;  // the end of the work list
+        const int seq = H.slot_seq[t % kSlots];
+        const int nst = a.p[(desc >> 24) & 1].K / kStageK;
+        const int b = seq & 1;
+        const uint32_t dcol = tmem + kDCol0 + b * kDCols + r * kNMax;
+        idesc = f16_idesc((((desc >> 8) & 0xff) + 15) & ~15);
+        // the accumulators are free once the epilogue two items back has read them
+        ok = wait_or_abort(smem_addr(&H.d_free[b]), (static_cast<uint32_t>(seq >> 1) & 1u) ^ 1u, a, abort);
+        for (int s = 0; s < nst && ok; ++s, ++t) {
+          const int ast = t % kAStages, slot = t % kSlots;
+          // the stage is in TMEM (the first stage's wait is above)
+          if (s > 0) {
+            ok = wait_or_abort(smem_addr(&H.a_full[ast]), static_cast<uint32_t>(t / kAStages) & 1u, a, abort);
             if (!ok) break;
           }
           tc_fence_after();
@@ -463,13 +501,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int n_cnt = 0, pos0 = 0, blk = 0;
     uint32_t xphase = 0;
     bool ok = true;
+    // A gate warp of a launch that also holds down items reports each finished item
+    // to its expert's counter (a device-scope release after its h stores), but one
+    // stage late, when those stores have long completed and the fence costs little;
+    // or at once when the next stage is not there yet, since the producer may be
+    // waiting for exactly this count before it issues more.
+    int sig_e = -1;
+    auto signal = [&]() {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a.gu_done + sig_e) : "memory");
+      sig_e = -1;
+    };
     for (int t = grp; ok; t += kGroups) {
       const int slot = t % kSlots;
-      ok = warp_wait(smem_addr(&H.slot_full[slot]), static_cast<uint32_t>(t / kSlots) & 1u, a, abort);
+      const uint32_t full = smem_addr(&H.slot_full[slot]);
+      const uint32_t fpar = static_cast<uint32_t>(t / kSlots) & 1u;
+      if (sig_e >= 0 && !__all_sync(0xffffffffu, mbar_test_wait(full, fpar))) signal();
+      ok = warp_wait(full, fpar, a, abort);
       if (!ok) break;
       const int desc = H.slot_desc[slot];
       const int seq = H.slot_seq[slot];
       if (desc < 0) {  // end of the work list: pass it on to the issuers, which learn of stages via a_full
+        if (sig_e >= 0) signal();
         // (only after the stage that last used this TMEM stage was consumed, so a_full never runs a
         // phase ahead)
         if (t >= kAStages) {
@@ -483,11 +537,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       const int s = desc & 0xff;
       n_cnt = (desc >> 8) & 0xff;
-      blk = desc >> 16;
-      pos0 = H.slot_pos0[slot];
+      blk = (desc >> 16) & 0xff;
+      const int pj = (desc >> 24) & 1;
+      const int aux = H.slot_pos0[slot];
+      pos0 = aux & ((1 << 22) - 1);
+      const int e = aux >> 22;
       const uint8_t* st = ring + slot * kSlotBytes;
       // (scale, zero) of row m for the group(s) of this stage (every slot carries them)
-      const int ngrp = max(groups_in_stage(s, a.g), 1);
+      const int ngrp = max(groups_in_stage(s, a.p[pj].g), 1);
       const uint32_t* sz = reinterpret_cast<const uint32_t*>(st + kCodeOff - kSzBytes * ngrp);
       {
         const __half2 v0 = bits_h2(sz[m]);
@@ -526,7 +583,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&H.a_full[ast]));
-      if (s == nst - 1) {
+      if (sig_e >= 0) signal();
+      if ((desc >> 25) & 1) {  // the item's last stage
         // ------------------------------------------------------------ accumulators
         const int b = seq & 1;
         ok = warp_wait(smem_addr(&H.d_full[b]), static_cast<uint32_t>(seq >> 1) & 1u, a, abort);
@@ -550,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&H.d_free[b]));  // the item after next may accumulate here
         // ------------------------------------------------------------ epilogue
-        if (kEpi == 0) {
+        if (pj == 0) {
           // rows 0..63 gate j = 64*blk + m, rows 64..127 up j = 64*blk + m - 64; the up rows
           // reach the gate rows' threads through this group's exchange area (bounded
           // mbarriers, not a named barrier, so a timed-out warp cannot strand the others)
@@ -576,12 +634,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               for (int c = 0; c < 4; ++c) {
                 const int n = 4 * i + c;
                 if (n < n_cnt)
-                  a.h_out[static_cast<size_t>(pos0 + n) * a.f + j] =
+                  a.h[static_cast<size_t>(pos0 + n) * a.f + j] =
                       __half_as_ushort(__float2half_rn(gelu(acc[n], a.act) * up[c]));
               }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&H.xch_done[grp]));
+            if (a.last == 1) sig_e = e;  // reported one stage later (see signal above)
           }
           xphase ^= 1u;
         } else {
@@ -599,13 +658,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
   }
+  // The last CTA to finish clears the work counter for the next launch on this
+  // workspace: by then every CTA has seen the list exhausted and claims no more.
+  if (tid == 0 && atomicAdd(a.done_ctas, 1) == static_cast<int>(gridDim.x) - 1) {
+    *a.counter = 0;
+    *a.done_ctas = 0;
+  }
 }
 
 // Token rows of every (token, expert) pair, copied in expert-sorted order:
-// xs[pos] = x[pair_list[pos] / k].  One warp per row, 16-byte accesses.
+// xs[pos] = x[pair_list[pos] / k].  One warp per row, 16-byte accesses.  Also
+// clears the per-expert gate_up counters that the GEMM launch after it counts up.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ pair_list, int P, int k, int d,
-                                                          uint16_t* __restrict__ xs) {
+                                                          uint16_t* __restrict__ xs, int32_t* __restrict__ gu_done,
+                                                          int E) {
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) gu_done[e] = 0;
   const int pos = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (pos >= P) return;
   const int t = pair_list[pos] / k;
@@ -617,7 +686,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-// 2-D tensor map over rows x cols fp16 (row-major), box 64 columns x 16 rows, 128B swizzle.
+// 2-D tensor map over rows x cols fp16 (row-major), box 64 columns x 32 rows, 128B swizzle.
 bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
@@ -640,13 +709,11 @@ bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
 }  // namespace
 
 cudaError_t init_gemm_kernels(int* blocks_per_sm) {
-  for (const void* fn : {reinterpret_cast<const void*>(expert_gemm_tc_kernel<0>),
-                         reinterpret_cast<const void*>(expert_gemm_tc_kernel<1>)}) {
-    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (err != cudaSuccess) return err;
-  }
+  const void* fn = reinterpret_cast<const void*>(expert_gemm_tc_kernel);
+  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (err != cudaSuccess) return err;
   // Two CTAs per SM: shared memory, registers (launch bounds) and tensor memory
   // (2 x 256 of 512 columns) all allow exactly two.
   *blocks_per_sm = kCtasPerSm;
@@ -654,45 +721,46 @@ cudaError_t init_gemm_kernels(int* blocks_per_sm) {
 }
 
 cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, const int32_t* expert_offsets,
-                               const int32_t* pair_list, const uint8_t* w, uint16_t* h, float* y, WsHeader* hdr,
-                               int grid, cudaStream_t st) {
+                               const int32_t* pair_list, const uint8_t* w_gate_up, const uint8_t* w_down,
+                               const GemmWorkspace& ws, int grid, cudaStream_t st) {
   const int P = static_cast<int>(s.pairs());
   TcArgs a{};
-  a.w = w;
+  const int K[2] = {s.d, s.f}, g[2] = {s.g1, s.g2}, nb[2] = {s.f / 64, s.d / kBlockRows};
+  const uint8_t* w[2] = {w_gate_up, w_down};
+  for (int pj = 0; pj < 2; ++pj) {
+    a.p[pj].w = w[pj];
+    a.p[pj].K = K[pj];
+    a.p[pj].g = g[pj];
+    a.p[pj].nblocks = nb[pj];
+    a.p[pj].block_bytes = int64_t(kBlockRows) * K[pj] / 2 + int64_t(kBlockRows) * (K[pj] / g[pj]) * 4;
+    a.p[pj].expert_bytes = a.p[pj].block_bytes * nb[pj];
+  }
+  a.first = (which & kGemmGateUp) ? 0 : 1;
+  a.last = (which & kGemmDown) ? 1 : 0;
+  if (which == 0 || a.first > a.last) return cudaErrorInvalidValue;
   a.offsets = expert_offsets;
   a.pair_list = pair_list;
   a.E = s.E;
   a.f = s.f;
   a.d = s.d;
   a.act = s.act;
-  a.err = &hdr->error;
-  a.h_out = h;
-  a.y_out = y;
-  CUtensorMap bmap;
-  if (which == 0) {  // gate_up: rows 2f in f/64 blocks of 64 gate + 64 up rows, K = d
-    // the token rows are first copied in expert order into the (still unused) y region
-    uint16_t* xs = reinterpret_cast<uint16_t*>(y);
-    gather_rows_kernel<<<(P + 7) / 8, 256, 0, st>>>(x, pair_list, P, s.k, s.d, xs);
+  a.err = &ws.hdr->error;
+  a.h = ws.h;
+  a.y_out = ws.y;
+  // gate_up launches (alone or fused) and down-only launches keep separate counters
+  const int c = a.first == 0 ? 0 : 1;
+  a.counter = &ws.hdr->next_item[c];
+  a.done_ctas = &ws.hdr->done_ctas[c];
+  a.gu_done = ws.gu_done;
+  if (which & kGemmGateUp) {
+    // the token rows are first copied in expert order
+    gather_rows_kernel<<<(P + 7) / 8, 256, 0, st>>>(x, pair_list, P, s.k, s.d, ws.xs, ws.gu_done, s.E);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    if (!make_row_map(&bmap, xs, P, s.d)) return cudaErrorInvalidValue;
-    a.K = s.d;
-    a.g = s.g1;
-    a.nblocks = s.f / 64;
-    a.counter = &hdr->next_item[0];
-    a.counter_to_reset = &hdr->next_item[1];
-  } else {           // down: rows d in d/128 blocks, K = f
-    if (!make_row_map(&bmap, h, P, s.f)) return cudaErrorInvalidValue;
-    a.K = s.f;
-    a.g = s.g2;
-    a.nblocks = s.d / kBlockRows;
-    a.counter = &hdr->next_item[1];
-    a.counter_to_reset = &hdr->next_item[0];
   }
-  a.block_bytes = int64_t(kBlockRows) * a.K / 2 + int64_t(kBlockRows) * (a.K / a.g) * 4;
-  a.expert_bytes = a.block_bytes * a.nblocks;
-  if (which == 0) expert_gemm_tc_kernel<0><<<grid, kThreads, kSmemBytes, st>>>(a, bmap);
-  else expert_gemm_tc_kernel<1><<<grid, kThreads, kSmemBytes, st>>>(a, bmap);
+  CUtensorMap map_x, map_h;
+  if (!make_row_map(&map_x, ws.xs, P, s.d) || !make_row_map(&map_h, ws.h, P, s.f)) return cudaErrorInvalidValue;
+  expert_gemm_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(a, map_x, map_h);
   return cudaGetLastError();
 }
 

@@ -21,9 +21,10 @@ constexpr int64_t kMaxPairs = int64_t(1) << 22;
 // Workspace header (bytes at the start of the workspace).
 struct WsHeader {
   int32_t error;          // sticky moe_w4a16_status of device-side failures
-  int32_t next_item[2];   // dynamic work counters of the gate_up (0) and down (1) kernels
+  int32_t next_item[2];   // work counters of GEMM launches with gate_up items (0) and of down-only launches (1)
+  int32_t done_ctas[2];   // CTAs of such a launch that have finished (the last resets both)
   uint32_t route_ticket;  // CTAs of the routing launch that have finished their top-k (reset by the last)
-  int32_t pad[60];
+  int32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -32,12 +33,31 @@ struct Dims {
   int64_t pairs() const { return int64_t(T) * k; }
 };
 
-// Workspace carve-up.
-inline size_t ws_h_offset() { return sizeof(WsHeader); }
+// Workspace carve-up: header | per-expert gate_up counters | h | xs | y.
+inline size_t ws_cnt_offset() { return sizeof(WsHeader); }
+inline size_t ws_h_offset() { return ws_cnt_offset() + size_t(kMaxExperts) * 4; }
 inline size_t ws_h_bytes(const Dims& s) { return size_t(s.pairs()) * s.f * 2; }
-inline size_t ws_y_offset(const Dims& s) { return (ws_h_offset() + ws_h_bytes(s) + 255) / 256 * 256; }
+inline size_t ws_xs_offset(const Dims& s) { return (ws_h_offset() + ws_h_bytes(s) + 255) / 256 * 256; }
+inline size_t ws_xs_bytes(const Dims& s) { return size_t(s.pairs()) * s.d * 2; }
+inline size_t ws_y_offset(const Dims& s) { return (ws_xs_offset(s) + ws_xs_bytes(s) + 255) / 256 * 256; }
 inline size_t ws_y_bytes(const Dims& s) { return size_t(s.pairs()) * s.d * 4; }
 inline size_t ws_total(const Dims& s) { return ws_y_offset(s) + ws_y_bytes(s); }
+
+// Device pointers of one workspace's parts.
+struct GemmWorkspace {
+  WsHeader* hdr;
+  int32_t* gu_done;  // [kMaxExperts]
+  uint16_t* h;       // [T*k][f]
+  uint16_t* xs;      // [T*k][d]
+  float* y;          // [T*k][d]
+};
+inline GemmWorkspace carve_workspace(void* ws, const Dims& s) {
+  auto* base = static_cast<uint8_t*>(ws);
+  return GemmWorkspace{static_cast<WsHeader*>(ws), reinterpret_cast<int32_t*>(base + ws_cnt_offset()),
+                       reinterpret_cast<uint16_t*>(base + ws_h_offset()),
+                       reinterpret_cast<uint16_t*>(base + ws_xs_offset(s)),
+                       reinterpret_cast<float*>(base + ws_y_offset(s))};
+}
 
 // Kernel launchers (defined in the .cu files).  Each returns the launch status.
 cudaError_t launch_route(const Dims& s, const float* logits, int32_t* topk_idx, float* topk_w,
@@ -47,10 +67,13 @@ cudaError_t launch_route(const Dims& s, const float* logits, int32_t* topk_idx, 
 // CTAs fit on one SM.  Called once per device before the first launch there.
 cudaError_t init_gemm_kernels(int* blocks_per_sm);
 
-// which = 0: gate_up GEMM (x -> h), which = 1: down GEMM (h -> y).
+// Expert GEMMs.  which is a mask: kGemmGateUp (x -> h, with the copy of the
+// token rows in expert order), kGemmDown (h -> y), or both in one launch (down
+// items wait for their expert's gate_up items).
+constexpr int kGemmGateUp = 1, kGemmDown = 2;
 cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, const int32_t* expert_offsets,
-                               const int32_t* pair_list, const uint8_t* w, uint16_t* h, float* y, WsHeader* hdr,
-                               int grid, cudaStream_t st);
+                               const int32_t* pair_list, const uint8_t* w_gate_up, const uint8_t* w_down,
+                               const GemmWorkspace& ws, int grid, cudaStream_t st);
 
 cudaError_t launch_combine(const Dims& s, const float* topk_w, const float* y, const float* gamma, float eps,
                            uint16_t* out, cudaStream_t st);
