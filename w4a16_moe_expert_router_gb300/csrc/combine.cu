@@ -14,6 +14,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -27,6 +28,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restri
                                                            const float* __restrict__ gamma, float eps,
                                                            uint16_t* __restrict__ out) {
   __shared__ float warp_ss[kThreads / 32];
+  grid_dependents_launch();
+  grid_dependency_wait();  // the expert outputs y of the launch before
   const int t = blockIdx.x, tid = threadIdx.x;
   const int n4 = d >> 2;
   float wr[kMaxTopK];
@@ -93,9 +96,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restri
 
 cudaError_t launch_combine(const Dims& s, const float* topk_w, const float* y, const float* gamma, float eps,
                            uint16_t* out, cudaStream_t st) {
-  if (gamma) combine_kernel<true><<<s.T, kThreads, 0, st>>>(topk_w, y, s.d, s.k, gamma, eps, out);
-  else combine_kernel<false><<<s.T, kThreads, 0, st>>>(topk_w, y, s.d, s.k, nullptr, eps, out);
-  return cudaGetLastError();
+  if (gamma) return launch_pdl(combine_kernel<true>, dim3(s.T), dim3(kThreads), 0, st, topk_w, y, s.d, s.k, gamma, eps, out);
+  return launch_pdl(combine_kernel<false>, dim3(s.T), dim3(kThreads), 0, st, topk_w, y, s.d, s.k,
+                    static_cast<const float*>(nullptr), eps, out);
 }
 
 }  // namespace moe

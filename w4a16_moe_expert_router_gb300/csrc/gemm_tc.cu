@@ -38,8 +38,8 @@
 //               occupies the issuing thread for ~50-90 cycles whatever N is, so
 //               two issuers share that cost; each commits once per stage
 //               (releasing the slot and the TMEM stage) and once per item;
-//   warps 3-10  two dequant groups of four warps, one warp per TMEM lane
-//               quadrant; group G takes the stages t = G mod 2: each thread owns
+//   warps 3-14  three dequant groups of four warps, one warp per TMEM lane
+//               quadrant; group G takes the stages t = G mod 3: each thread owns
 //               one GEMM row and writes the row's 64 weights of the stage into
 //               the stage's TMEM buffer (one tcgen05.st of 32 columns).  The
 //               group that gets an item's last stage reads the row's two
@@ -62,7 +62,7 @@
 namespace moe {
 namespace {
 
-constexpr int kGroups = 2;                     // dequant groups (four warps each, one per lane quadrant)
+constexpr int kGroups = 3;                     // dequant groups (four warps each, one per lane quadrant)
 constexpr int kDqWarps = 4 * kGroups;
 constexpr int kIssuers = 2;                    // MMA issuers: k16 steps {0,1} and {2,3} of every stage
 constexpr int kFirstDqWarp = 1 + kIssuers;
@@ -87,7 +87,7 @@ constexpr int kCodeOff = kBBytes + 2 * kSzBytes;      // codes always land here
 constexpr int kSlotBytes = 10240;                     // multiple of 1024
 static_assert(kCodeOff + kCodeBytes <= kSlotBytes && kSlotBytes % 1024 == 0, "slot layout");
 constexpr int kXchStride = kNMax + 4;          // floats per exchanged row (bank-conflict padding)
-constexpr int kXchBytes = kGroups * 64 * kXchStride * 4;  // one exchange area per group
+constexpr int kXchBytes = kDBufs * 64 * kXchStride * 4;   // one exchange area per accumulator set
 constexpr int kHeaderBytes = 4096;
 constexpr int kRingOff = (kHeaderBytes + kXchBytes + 1023) / 1024 * 1024;
 constexpr int kSmemBytes = 1024 + kRingOff + kSlots * kSlotBytes;  // +1024 for alignment
@@ -124,8 +124,8 @@ struct __align__(8) TcHeader {
   uint64_t d_full[kDBufs];      // an item's accumulators are final (one commit per issuer)
   uint64_t d_free[kDBufs];      // the epilogue has read them (4 warps)
   uint64_t drain;
-  uint64_t xch_ready[kGroups];  // the 2 up-row warps of a group have written their rows
-  uint64_t xch_done[kGroups];   // the 2 gate-row warps of a group have read them
+  uint64_t xch_ready[kDBufs];   // the 2 up-row warps of an item have written their rows
+  uint64_t xch_done[kDBufs];    // the 2 gate-row warps of an item have read them
   int slot_desc[kSlots];        // stage | tokens << 8 | block << 16 | proj << 24 | last << 25, or -1 at the end
   int slot_pos0[kSlots];        // first expert-sorted row of the item's tokens | expert << 22
   int slot_seq[kSlots];         // the item's sequence number within this CTA
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(smem_addr(&H.slot_empty[i]), 4 + kIssuers);  // the stage's 4 dequant warps + 2 commits
     }
     for (int i = 0; i < kAStages; ++i) mbar_init(smem_addr(&H.a_full[i]), 4);
-    for (int i = 0; i < kGroups; ++i) {
+    for (int i = 0; i < kDBufs; ++i) {
       mbar_init(smem_addr(&H.xch_ready[i]), 2);
       mbar_init(smem_addr(&H.xch_done[i]), 2);
     }
@@ -317,6 +317,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  // everything above is set-up; the routing arrays, the row copy and h come from earlier launches
+  grid_dependents_launch();
+  grid_dependency_wait();
   if (warp == 2) {  // items per expert = blocks * ceil(n_e / 32); exclusive scans, 8 experts per lane
     for (int pj = 0; pj < 2; ++pj) {
       const int nb = a.p[pj].nblocks;
@@ -496,10 +499,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int q = warp & 3;              // TMEM lane quadrant (rows 32q .. 32q+31)
     const int m = 32 * q + lane;         // GEMM row within the 128-row block
     const uint32_t lane_bits = static_cast<uint32_t>(32 * q) << 16;
-    float* xch = xch_all + grp * 64 * kXchStride;
     __half2 z0 = bits_h2(0u), z1 = bits_h2(0u), s0 = bits_h2(0u), s1 = bits_h2(0u);  // current group(s) of row m
     int n_cnt = 0, pos0 = 0, blk = 0;
-    uint32_t xphase = 0;
     bool ok = true;
     // A gate warp of a launch that also holds down items reports each finished item
     // to its expert's counter (a device-scope release after its h stores), but one
@@ -610,19 +611,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // ------------------------------------------------------------ epilogue
         if (pj == 0) {
           // rows 0..63 gate j = 64*blk + m, rows 64..127 up j = 64*blk + m - 64; the up rows
-          // reach the gate rows' threads through this group's exchange area (bounded
-          // mbarriers, not a named barrier, so a timed-out warp cannot strand the others)
+          // reach the gate rows' threads through the exchange area of the item's accumulator
+          // set (bounded mbarriers, not a named barrier, so a timed-out warp cannot strand the
+          // others).  A CTA's gate_up items come first in its sequence, so item seq is the
+          // (seq >> 1)-th user of area seq & 1.
+          float* xch = xch_all + b * 64 * kXchStride;
+          const uint32_t xphase = static_cast<uint32_t>(seq >> 1) & 1u;
           if (q >= 2) {
-            ok = warp_wait(smem_addr(&H.xch_done[grp]), xphase ^ 1u, a, abort);  // previous reads finished
+            ok = warp_wait(smem_addr(&H.xch_done[b]), xphase ^ 1u, a, abort);  // previous reads finished
             if (!ok) break;
             float4* dst = reinterpret_cast<float4*>(xch + (m - 64) * kXchStride);
 #pragma unroll
             for (int i = 0; i < kNMax / 4; ++i)
               dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&H.xch_ready[grp]));
+            if (lane == 0) mbar_arrive(smem_addr(&H.xch_ready[b]));
           } else {
-            ok = warp_wait(smem_addr(&H.xch_ready[grp]), xphase, a, abort);
+            ok = warp_wait(smem_addr(&H.xch_ready[b]), xphase, a, abort);
             if (!ok) break;
             const float4* up4 = reinterpret_cast<const float4*>(xch + m * kXchStride);
             const int j = 64 * blk + m;
@@ -639,10 +644,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
               }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&H.xch_done[grp]));
+            if (lane == 0) mbar_arrive(smem_addr(&H.xch_done[b]));
             if (a.last == 1) sig_e = e;  // reported one stage later (see signal above)
           }
-          xphase ^= 1u;
         } else {
           const int i_row = kBlockRows * blk + m;
 #pragma unroll
@@ -673,6 +677,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ pair_list, int P, int k, int d,
                                                           uint16_t* __restrict__ xs, int32_t* __restrict__ gu_done,
                                                           int E) {
+  grid_dependents_launch();
+  grid_dependency_wait();  // pair_list of the routing launch
   if (blockIdx.x == 0)
     for (int e = threadIdx.x; e < E; e += blockDim.x) gu_done[e] = 0;
   const int pos = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -754,14 +760,13 @@ cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, cons
   a.gu_done = ws.gu_done;
   if (which & kGemmGateUp) {
     // the token rows are first copied in expert order
-    gather_rows_kernel<<<(P + 7) / 8, 256, 0, st>>>(x, pair_list, P, s.k, s.d, ws.xs, ws.gu_done, s.E);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(gather_rows_kernel, dim3((P + 7) / 8), dim3(256), 0, st, x, pair_list, P, s.k, s.d,
+                                 ws.xs, ws.gu_done, s.E);
     if (err != cudaSuccess) return err;
   }
   CUtensorMap map_x, map_h;
   if (!make_row_map(&map_x, ws.xs, P, s.d) || !make_row_map(&map_h, ws.h, P, s.f)) return cudaErrorInvalidValue;
-  expert_gemm_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(a, map_x, map_h);
-  return cudaGetLastError();
+  return launch_pdl(expert_gemm_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, a, map_x, map_h);
 }
 
 }  // namespace moe

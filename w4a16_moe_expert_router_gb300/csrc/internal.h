@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "moe_w4a16.h"
 
 namespace moe {
@@ -57,6 +59,26 @@ inline GemmWorkspace carve_workspace(void* ws, const Dims& s) {
                        reinterpret_cast<uint16_t*>(base + ws_h_offset()),
                        reinterpret_cast<uint16_t*>(base + ws_xs_offset(s)),
                        reinterpret_cast<float*>(base + ws_y_offset(s))};
+}
+
+// Launches kernel<<<grid, block, smem, st>>>(args...) allowing programmatic
+// dependent launch: the kernel may start while the previous kernel on the
+// stream finishes, and waits for it (griddepcontrol.wait) before it touches
+// anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Kernel launchers (defined in the .cu files).  Each returns the launch status.

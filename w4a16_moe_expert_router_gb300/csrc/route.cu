@@ -174,6 +174,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
                                                               int32_t* __restrict__ pair_list,
                                                               uint32_t* __restrict__ ticket) {
   __shared__ int is_last;
+  grid_dependents_launch();  // the next launch may set up meanwhile; it waits for this one
+  grid_dependency_wait();    // logits, and the routing arrays an earlier launch may still read
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
   if (t < T)
@@ -194,9 +196,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __res
 cudaError_t launch_route(const Dims& s, const float* logits, int32_t* topk_idx, float* topk_w,
                          int32_t* expert_offsets, int32_t* pair_list, WsHeader* hdr, cudaStream_t st) {
   const int grid = (s.T + kRouteWarps - 1) / kRouteWarps;
-  route_kernel<<<grid, kRouteThreads, 0, st>>>(logits, s.T, s.E, s.k, topk_idx, topk_w, expert_offsets, pair_list,
-                                               &hdr->route_ticket);
-  return cudaGetLastError();
+  return launch_pdl(route_kernel, dim3(grid), dim3(kRouteThreads), 0, st, logits, s.T, s.E, s.k, topk_idx, topk_w,
+                    expert_offsets, pair_list, &hdr->route_ticket);
 }
 
 }  // namespace moe
