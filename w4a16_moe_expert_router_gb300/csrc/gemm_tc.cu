@@ -14,11 +14,12 @@
 // straight on with down work instead of idling until the slowest CTA finishes.
 // The same kernel also runs one projection alone (the separate C entry points).
 //
-// Arithmetic: each weight is formed as w = fp16(fp16(q - z) * s): the offset
-// removal and q - z are exact in fp16 (unless |q - z| >= 8 needs a 12th
-// significand bit), the product with the scale is rounded once, and the tensor
-// core multiplies w with the fp16 activations into an fp32 accumulator that stays
-// in tensor memory for the whole contraction.
+// Arithmetic: the zero-point is split into its nearest integer zr and the rest
+// zf = z - zr, and each weight is formed as w = fp16((q - zr) * s - fp16(zf * s)):
+// q - zr is exact in fp16, the fused multiply-add rounds once, and the rounding of
+// zf * s (|zf| <= 1/2) adds at most a few 1e-6.  The tensor core multiplies w with
+// the fp16 activations into an fp32 accumulator that stays in tensor memory for
+// the whole contraction.
 //
 // Roles of the persistent CTA (two per SM, 256 tensor-memory columns each; work
 // items = (expert, 128-row block, chunk of <= 32 tokens) taken from a global
@@ -227,18 +228,37 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Per-(row, group) constants of the dequantiser: the zero-point split into its
+// nearest integer zr and the rest zf = z - zr (exact in fp16), so that
+// (q - z) * s = (q - zr) * s - zf * s.
+struct DqGroup {
+  __half2 zb1024;  // 1024 + zr (exact)
+  __half2 zb64;    // 64 + zr (exact)
+  __half2 s;       // scale
+  __half2 c;       // -fp16(zf * s)
+};
+__device__ __forceinline__ DqGroup dq_group(__half2 s, __half2 z) {
+  const __half2 zr = h2rint(z);
+  const __half2 zf = __hsub2(z, zr);
+  DqGroup g;
+  g.zb1024 = __hadd2(zr, bits_h2(0x64006400u));
+  g.zb64 = __hadd2(zr, bits_h2(0x54005400u));
+  g.s = s;
+  g.c = __hneg2(__hmul2(zf, s));
+  return g;
+}
+
 // 8 codes of one row (nibbles in column order 0,2,4,6,1,3,5,7) -> four f16x2 weights
-// w = fp16(fp16(q - z) * s) for columns (k, k+1), (k+2, k+3), (k+4, k+5), (k+6, k+7).
-// (1024 + q) and (64 + q) come from OR-ing exponent bits onto the nibbles; one fp16
-// add removes the offset exactly, one subtract forms q - z (exact unless |q - z| >= 8
-// needs a 12th significand bit) and one multiply rounds the product once.
-__device__ __forceinline__ void dequant_row8(uint32_t w, __half2 z, __half2 s, uint32_t* out) {
+// w = fp16((q - zr) * s - fp16(zf * s)) for columns (k, k+1), (k+2, k+3), (k+4, k+5),
+// (k+6, k+7).  (1024 + q) and (64 + q) come from OR-ing exponent bits onto the
+// nibbles; one fp16 subtract of (1024 + zr) or (64 + zr) gives q - zr exactly (both
+// operands are integers in fp16), and one fused multiply-add rounds the weight once.
+__device__ __forceinline__ void dequant_row8(uint32_t w, const DqGroup& g, uint32_t* out) {
   const uint32_t w8 = w >> 8;
-  const __half2 m1024 = bits_h2(0xe400e400u), m64 = bits_h2(0xd400d400u);
-  out[0] = h2_bits(__hmul2(__hsub2(__hadd2(bits_h2(and_or(w, 0x000f000fu, 0x64006400u)), m1024), z), s));
-  out[1] = h2_bits(__hmul2(__hsub2(__hadd2(bits_h2(and_or(w, 0x00f000f0u, 0x54005400u)), m64), z), s));
-  out[2] = h2_bits(__hmul2(__hsub2(__hadd2(bits_h2(and_or(w8, 0x000f000fu, 0x64006400u)), m1024), z), s));
-  out[3] = h2_bits(__hmul2(__hsub2(__hadd2(bits_h2(and_or(w8, 0x00f000f0u, 0x54005400u)), m64), z), s));
+  out[0] = h2_bits(__hfma2(__hsub2(bits_h2(and_or(w, 0x000f000fu, 0x64006400u)), g.zb1024), g.s, g.c));
+  out[1] = h2_bits(__hfma2(__hsub2(bits_h2(and_or(w, 0x00f000f0u, 0x54005400u)), g.zb64), g.s, g.c));
+  out[2] = h2_bits(__hfma2(__hsub2(bits_h2(and_or(w8, 0x000f000fu, 0x64006400u)), g.zb1024), g.s, g.c));
+  out[3] = h2_bits(__hfma2(__hsub2(bits_h2(and_or(w8, 0x00f000f0u, 0x54005400u)), g.zb64), g.s, g.c));
 }
 
 __device__ __forceinline__ float gelu(float a, int act) {
@@ -499,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int q = warp & 3;              // TMEM lane quadrant (rows 32q .. 32q+31)
     const int m = 32 * q + lane;         // GEMM row within the 128-row block
     const uint32_t lane_bits = static_cast<uint32_t>(32 * q) << 16;
-    __half2 z0 = bits_h2(0u), z1 = bits_h2(0u), s0 = bits_h2(0u), s1 = bits_h2(0u);  // current group(s) of row m
+    DqGroup g0, g1;  // the dequantiser constants of the stage's group(s) for row m
     int n_cnt = 0, pos0 = 0, blk = 0;
     bool ok = true;
     // A gate warp of a launch that also holds down items reports each finished item
@@ -550,24 +570,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       {
         const __half2 v0 = bits_h2(sz[m]);
         const __half2 v1 = ngrp > 1 ? bits_h2(sz[kBlockRows + m]) : v0;
-        s0 = __low2half2(v0);
-        s1 = __low2half2(v1);
-        z0 = __high2half2(v0);
-        z1 = __high2half2(v1);
+        g0 = dq_group(__low2half2(v0), __high2half2(v0));
+        g1 = dq_group(__low2half2(v1), __high2half2(v1));
       }
       // this row's 64 codes: two 16-byte halves, [half][row][16 B]; with groups of 32
       // the second half belongs to the stage's second group
       const uint4 c0 = *reinterpret_cast<const uint4*>(st + kCodeOff + m * 16);
       const uint4 c1 = *reinterpret_cast<const uint4*>(st + kCodeOff + kBlockRows * 16 + m * 16);
       uint32_t w[32];
-      dequant_row8(c0.x, z0, s0, w + 0);
-      dequant_row8(c0.y, z0, s0, w + 4);
-      dequant_row8(c0.z, z0, s0, w + 8);
-      dequant_row8(c0.w, z0, s0, w + 12);
-      dequant_row8(c1.x, z1, s1, w + 16);
-      dequant_row8(c1.y, z1, s1, w + 20);
-      dequant_row8(c1.z, z1, s1, w + 24);
-      dequant_row8(c1.w, z1, s1, w + 28);
+      dequant_row8(c0.x, g0, w + 0);
+      dequant_row8(c0.y, g0, w + 4);
+      dequant_row8(c0.z, g0, w + 8);
+      dequant_row8(c0.w, g0, w + 12);
+      dequant_row8(c1.x, g1, w + 16);
+      dequant_row8(c1.y, g1, w + 20);
+      dequant_row8(c1.z, g1, w + 24);
+      dequant_row8(c1.w, g1, w + 28);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&H.slot_empty[slot]));  // codes and scales are in registers
       const int ast = t % kAStages;
