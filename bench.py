@@ -359,7 +359,7 @@ def run_ours(args, rank, world, local):
         },
         "e2e": {"value": wl.tokens * KE * world / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE},
-        "gpu_launches": K * layers * 4,  # route, row copy, expert GEMMs, combine
+        "gpu_launches": K * layers * 5,  # top-k, grouping, row copy, expert GEMMs, combine
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -109,8 +109,9 @@ typedef struct {
 /* Bytes of device workspace that moe_w4a16_route and moe_w4a16_forward need for
  * this shape (0 on an invalid shape).  The workspace holds the intermediate
  * activations h (fp16 [T*k][f]), the token rows copied in expert order
- * (fp16 [T*k][d]) and per-pair expert outputs (fp32 [T*k][d]) plus a small
- * header (error word, work counters).  It must be initialised once with
+ * (fp16 [T*k][d]), per-pair expert outputs (fp32 [T*k][d]) and routing scratch
+ * (per-CTA expert counts, per-pair ranks) plus a small header (error word, work
+ * counters).  It must be initialised once with
  * moe_w4a16_workspace_init before its first use; later calls leave it ready. */
 MOE_W4A16_API size_t moe_w4a16_workspace_bytes(const moe_w4a16_shape* shape);
 

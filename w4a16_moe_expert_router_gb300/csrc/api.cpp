@@ -105,7 +105,7 @@ moe_w4a16_status moe_w4a16_route(const moe_w4a16_shape* shape, const float* logi
   const DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != MOE_W4A16_OK) return st;
   return cuda_status(moe::launch_route(s, logits, out->topk_idx, out->topk_w, out->expert_offsets, out->pair_list,
-                                       static_cast<moe::WsHeader*>(workspace), static_cast<cudaStream_t>(stream)));
+                                       workspace, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

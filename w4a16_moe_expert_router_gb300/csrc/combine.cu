@@ -19,8 +19,8 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kMaxVec = 8;  // float4 per thread: d <= 8192
+constexpr int kThreads = 512;
+constexpr int kMaxVec = 4;  // float4 per thread: d <= 8192
 
 template <bool kNorm>
 __global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restrict__ topk_w,
@@ -42,16 +42,19 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restri
   for (int j = 0; j < kMaxVec; ++j) {
     const int i4 = tid + kThreads * j;
     if (i4 < n4) {
-      float4 v = y4[i4];
-      float4 acc = make_float4(wr[0] * v.x, wr[0] * v.y, wr[0] * v.z, wr[0] * v.w);
+      // all k rows' values are requested before the first is used
+      float4 v[kMaxTopK];
+#pragma unroll
+      for (int r = 0; r < kMaxTopK; ++r)
+        if (r < k) v[r] = y4[static_cast<size_t>(r) * n4 + i4];
+      float4 acc = make_float4(wr[0] * v[0].x, wr[0] * v[0].y, wr[0] * v[0].z, wr[0] * v[0].w);
 #pragma unroll
       for (int r = 1; r < kMaxTopK; ++r) {
         if (r < k) {
-          v = y4[static_cast<size_t>(r) * n4 + i4];
-          acc.x = fmaf(wr[r], v.x, acc.x);
-          acc.y = fmaf(wr[r], v.y, acc.y);
-          acc.z = fmaf(wr[r], v.z, acc.z);
-          acc.w = fmaf(wr[r], v.w, acc.w);
+          acc.x = fmaf(wr[r], v[r].x, acc.x);
+          acc.y = fmaf(wr[r], v[r].y, acc.y);
+          acc.z = fmaf(wr[r], v[r].z, acc.z);
+          acc.w = fmaf(wr[r], v[r].w, acc.w);
         }
       }
       u[j] = acc;

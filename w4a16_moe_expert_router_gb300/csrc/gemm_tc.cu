@@ -378,6 +378,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       asm volatile("prefetch.tensormap [%0];" ::"l"(&map_h) : "memory");
     }
     int t = 0, seq = 0, sentinels = 0;
+    // every weight byte is read once: it leaves L2 first, so that h, y and the token rows stay
+    const uint64_t w_policy = l2_evict_first_policy();
     uint32_t issued_mask = 0;   // slots whose last phase carried copies
     uint32_t issued_par = 0;    // parity of that phase, one bit per slot
     bool ok = true;
@@ -442,14 +444,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const uint32_t dst = smem_addr(ring + slot * kSlotBytes);
             if (ngrp > 0) {
               mbar_arrive_expect_tx(full, seg + kBBoxRows * 128);
-              bulk_g2s(dst + kCodeOff - kSzBytes * ngrp, wsrc, seg, full);
+              bulk_g2s_hint(dst + kCodeOff - kSzBytes * ngrp, wsrc, seg, full, w_policy);
               sz_src = wsrc;
             } else {
               // a stage inside a group (groups of 128) gets a copy of the group's (scale, zero)
               // pairs (from L2) so that every slot is self-contained
               mbar_arrive_expect_tx(full, kSzBytes + seg + kBBoxRows * 128);
               bulk_g2s(dst + kCodeOff - kSzBytes, sz_src, kSzBytes, full);
-              bulk_g2s(dst + kCodeOff, wsrc, seg, full);
+              bulk_g2s_hint(dst + kCodeOff, wsrc, seg, full, w_policy);
             }
             tma_load_2d(dst, bmap, s * kStageK, pos0, full);
             wsrc += seg;
@@ -704,7 +706,20 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   const int t = pair_list[pos] / k;
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
   uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<size_t>(pos) * d);
-  for (int i = lane; i < d / 8; i += 32) dst[i] = src[i];
+  // up to 8 loads in flight per lane before the first store (d <= 8192: 32 per lane)
+  for (int i0 = 0; i0 < d / 8; i0 += 32 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * 32 + lane;
+      if (i < d / 8) v[j] = src[i];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * 32 + lane;
+      if (i < d / 8) dst[i] = v[j];
+    }
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;

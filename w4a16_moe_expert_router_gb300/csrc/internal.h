@@ -25,8 +25,7 @@ struct WsHeader {
   int32_t error;          // sticky moe_w4a16_status of device-side failures
   int32_t next_item[2];   // work counters of GEMM launches with gate_up items (0) and of down-only launches (1)
   int32_t done_ctas[2];   // CTAs of such a launch that have finished (the last resets both)
-  uint32_t route_ticket;  // CTAs of the routing launch that have finished their top-k (reset by the last)
-  int32_t pad[58];
+  int32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -35,7 +34,7 @@ struct Dims {
   int64_t pairs() const { return int64_t(T) * k; }
 };
 
-// Workspace carve-up: header | per-expert gate_up counters | h | xs | y.
+// Workspace carve-up: header | per-expert gate_up counters | h | xs | y | routing scratch.
 inline size_t ws_cnt_offset() { return sizeof(WsHeader); }
 inline size_t ws_h_offset() { return ws_cnt_offset() + size_t(kMaxExperts) * 4; }
 inline size_t ws_h_bytes(const Dims& s) { return size_t(s.pairs()) * s.f * 2; }
@@ -43,7 +42,11 @@ inline size_t ws_xs_offset(const Dims& s) { return (ws_h_offset() + ws_h_bytes(s
 inline size_t ws_xs_bytes(const Dims& s) { return size_t(s.pairs()) * s.d * 2; }
 inline size_t ws_y_offset(const Dims& s) { return (ws_xs_offset(s) + ws_xs_bytes(s) + 255) / 256 * 256; }
 inline size_t ws_y_bytes(const Dims& s) { return size_t(s.pairs()) * s.d * 4; }
-inline size_t ws_total(const Dims& s) { return ws_y_offset(s) + ws_y_bytes(s); }
+// routing scratch: per-CTA expert counts of the top-k launch (8 tokens per CTA), then the pairs' ranks
+inline size_t ws_route_offset(const Dims& s) { return (ws_y_offset(s) + ws_y_bytes(s) + 255) / 256 * 256; }
+inline size_t ws_route_hist_bytes(const Dims& s) { return size_t((s.T + 7) / 8) * s.E * 4; }
+inline size_t ws_route_bytes(const Dims& s) { return ws_route_hist_bytes(s) + size_t(s.pairs()) * 4; }
+inline size_t ws_total(const Dims& s) { return ws_route_offset(s) + ws_route_bytes(s); }
 
 // Device pointers of one workspace's parts.
 struct GemmWorkspace {
@@ -83,7 +86,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Kernel launchers (defined in the .cu files).  Each returns the launch status.
 cudaError_t launch_route(const Dims& s, const float* logits, int32_t* topk_idx, float* topk_w,
-                         int32_t* expert_offsets, int32_t* pair_list, WsHeader* hdr, cudaStream_t st);
+                         int32_t* expert_offsets, int32_t* pair_list, void* workspace, cudaStream_t st);
 
 // Sets the kernels' attributes on the current device and reports how many GEMM
 // CTAs fit on one SM.  Called once per device before the first launch there.

@@ -1,5 +1,5 @@
-// route.cu -- routing of a canvas in one launch: top-k experts per token,
-// softmax over the selected logits, and the per-expert pair lists.
+// route.cu -- routing of a canvas: top-k experts per token, softmax over the
+// selected logits, and the per-expert pair lists.
 //
 // Model card "srswti/axe-diffusion-ksl-xe", "what the model is": every token is
 // routed to its top-8 of 128 experts.  "The kernels we built": one launch then
@@ -7,11 +7,12 @@
 // stable counting sort (pair id ascending inside an expert) with no atomics on
 // positions, so the lists are identical from run to run.
 //
-// Every CTA ranks the experts of 32 tokens (one warp per token).  The CTA that
-// finishes last -- it learns so from a ticket counter in the workspace header,
-// taken after its top-k results are fenced -- then groups all pairs by expert.
-// No CTA waits for another, so the launch cannot stall however its CTAs are
-// scheduled.
+// Two launches.  The first ranks the experts of every token (one warp per
+// token, eight tokens per CTA, so even a 256-token canvas spreads over 32 SMs)
+// and, per CTA, counts its pairs per expert and ranks each pair among the
+// CTA's earlier pairs of the same expert.  The second, one CTA launched with
+// programmatic dependent launch, turns the per-CTA counts into positions
+// (exclusive scans over CTAs, then over experts) and places every pair.
 #include <cfloat>
 #include <climits>
 
@@ -21,29 +22,38 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteThreads = 1024;
-constexpr int kRouteWarps = kRouteThreads / 32;  // tokens per CTA
+constexpr int kTopkWarps = 8;        // tokens per CTA of the top-k launch
+constexpr int kGroupThreads = 1024;  // the grouping CTA
+constexpr int kScanSplit = kGroupThreads / kMaxExperts;  // threads per expert in the scan over CTAs
 
-// Router order: larger logit first; equal logits (fp32 compare, so -0 == +0)
-// go to the lower expert index.  An id of INT_MAX marks "no candidate".
-__device__ __forceinline__ bool ranks_before(float a, int ea, float b, int eb) {
-  if (ea == INT_MAX) return false;
-  if (eb == INT_MAX) return true;
-  return a > b || (a == b && ea < eb);
+// Router order as one unsigned key: a larger logit gives a larger key, -0 and
+// +0 give the same key (they compare equal as fp32 values); NaN ranks below
+// every number.  Equal keys go to the lower expert index.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  if (v != v) return 1u;
+  if (v == 0.f) v = 0.f;
+  const uint32_t b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
 // Top-k of one token's E logits by one warp (lane j holds experts j, j+32, ...;
 // E <= 256), then the softmax over the k selected logits, summed in rank order.
+// Each round takes the largest key over the warp (one reduction) and, among the
+// lanes holding it, the lowest expert index (a second reduction).
 __device__ __forceinline__ void topk_softmax_warp(const float* __restrict__ row, int E, int k, int lane,
-                                                  int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
+                                                  int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                                                  int* __restrict__ sel_out) {
   float v[kMaxExperts / 32];
+  uint32_t key[kMaxExperts / 32];
   uint32_t avail = 0;
 #pragma unroll
   for (int j = 0; j < kMaxExperts / 32; ++j) {
     const int e = lane + 32 * j;
     v[j] = 0.f;
+    key[j] = 0u;
     if (e < E) {
       v[j] = row[e];
+      key[j] = order_key(v[j]);
       avail |= 1u << j;
     }
   }
@@ -54,27 +64,23 @@ __device__ __forceinline__ void topk_softmax_warp(const float* __restrict__ row,
     sel_v[r] = 0.f;
     sel_e[r] = 0;
     if (r < k) {
+      // this lane's best remaining candidate: largest key, then lowest index
+      uint32_t bk = 0u;
+      int bj = -1;
       float bv = 0.f;
-      int be = INT_MAX;
 #pragma unroll
       for (int j = 0; j < kMaxExperts / 32; ++j)
-        if (((avail >> j) & 1u) && ranks_before(v[j], lane + 32 * j, bv, be)) {
+        if (((avail >> j) & 1u) && (bj < 0 || key[j] > bk)) {
+          bk = key[j];
+          bj = j;
           bv = v[j];
-          be = lane + 32 * j;
         }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ranks_before(ov, oe, bv, be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      // every lane now holds the same winner (the order is total)
-      if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
-      sel_v[r] = bv;
-      sel_e[r] = be;
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bj >= 0 ? bk : 0u);
+      const uint32_t cand = (bj >= 0 && bk == kmax) ? static_cast<uint32_t>(lane + 32 * bj) : 0xffffffffu;
+      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+      if (static_cast<int>(win & 31u) == lane) avail &= ~(1u << (win >> 5));
+      sel_e[r] = static_cast<int>(win);
+      sel_v[r] = __shfl_sync(0xffffffffu, bv, static_cast<int>(win & 31u));
     }
   }
   const float m = sel_v[0];
@@ -87,44 +93,88 @@ __device__ __forceinline__ void topk_softmax_warp(const float* __restrict__ row,
     if (r < k && r == lane) {
       idx_out[r] = sel_e[r];
       w_out[r] = expf(sel_v[r] - m) / den;
+      sel_out[r] = sel_e[r];
     }
 }
 
-// Stable grouping of the P pairs by expert, by one CTA of kRouteThreads.  Warp w
-// owns the contiguous pair range [w*chunk, (w+1)*chunk); pass 1 counts each
-// warp's pairs per expert, a scan over (expert, warp) turns the counts into
-// first positions, pass 2 places every pair at its warp's running position for
-// its expert.  Within a warp, pairs go in rounds of 32 in pair order and a pair's
-// rank among equal experts of its round is the number of lower lanes with the
-// same expert, so the order inside an expert is the pair order.
-__device__ __forceinline__ void group_pairs_block(const int32_t* __restrict__ topk_idx, int P, int E,
-                                                  int32_t* __restrict__ expert_offsets,
-                                                  int32_t* __restrict__ pair_list) {
-  __shared__ int cnt[kRouteWarps][kMaxExperts];  // per warp and expert: count, then next position
-  __shared__ int base[kMaxExperts + 1];
+// Top-k of 8 tokens per CTA, then the CTA's pairs (p = t*k + r, in order) counted
+// per expert (cta_hist[cta][e]) and ranked among the CTA's earlier pairs of the
+// same expert (local_rank[p]).
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                                int32_t* __restrict__ topk_idx,
+                                                                float* __restrict__ topk_w,
+                                                                int32_t* __restrict__ cta_hist,
+                                                                int32_t* __restrict__ local_rank) {
+  __shared__ int sel[kTopkWarps * kMaxTopK];
+  __shared__ int hist[kMaxExperts];
+  grid_dependents_launch();  // the grouping launch may set up meanwhile; it waits for this one
+  grid_dependency_wait();    // logits, and the routing arrays an earlier launch may still read
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < kRouteWarps * kMaxExperts; i += kRouteThreads) (&cnt[0][0])[i] = 0;
-  __syncthreads();
-  const int chunk = (P + kRouteWarps - 1) / kRouteWarps;
-  const int p_lo = warp * chunk, p_hi = min(P, p_lo + chunk);
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (int r0 = p_lo; r0 < p_hi; r0 += 32) {
-    const int p = r0 + lane;
-    int e = p < p_hi ? __ldcg(topk_idx + p) : -1;
-    if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) e = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && __popc(peers & lt_mask) == 0) cnt[warp][e] += __popc(peers);
-    __syncwarp();
+  for (int e = tid; e < E; e += kTopkWarps * 32) hist[e] = 0;
+  const int t = blockIdx.x * kTopkWarps + warp;
+  if (t < T) {
+    topk_softmax_warp(logits + static_cast<size_t>(t) * E, E, k, lane, topk_idx + static_cast<size_t>(t) * k,
+                      topk_w + static_cast<size_t>(t) * k, sel + warp * k);
+  } else if (lane < k) {
+    sel[warp * k + lane] = -1;
   }
   __syncthreads();
-  if (tid < E) {  // per expert: exclusive scan over the warps, total in tot
-    int run = 0;
-    for (int w = 0; w < kRouteWarps; ++w) {
-      const int c = cnt[w][tid];
-      cnt[w][tid] = run;
-      run += c;
+  const int npairs = kTopkWarps * k;  // <= 64
+  if (warp == 0) {
+    // the CTA's pairs in rounds of 32, in pair order: a pair's rank is the count of its expert
+    // in earlier rounds plus the lower lanes of its round with the same expert
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int r0 = 0; r0 < npairs; r0 += 32) {
+      const int i = r0 + lane;
+      int e = i < npairs ? sel[i] : -1;
+      if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0) local_rank[static_cast<size_t>(blockIdx.x) * npairs + i] = hist[e] + __popc(peers & lt_mask);
+      __syncwarp();
+      if (e >= 0 && (peers & lt_mask) == 0) hist[e] += __popc(peers);
+      __syncwarp();
     }
-    base[tid] = run;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kTopkWarps * 32) cta_hist[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+// One CTA: per expert, the exclusive scan of the per-CTA counts over the CTAs
+// (written back in place), the expert offsets (exclusive scan over experts), and
+// every pair placed at offset + earlier CTAs' count + its rank in its CTA.
+__global__ void __launch_bounds__(kGroupThreads) group_kernel(const int32_t* __restrict__ topk_idx, int P, int E,
+                                                              int k, int nctas, int32_t* __restrict__ cta_hist,
+                                                              const int32_t* __restrict__ local_rank,
+                                                              int32_t* __restrict__ expert_offsets,
+                                                              int32_t* __restrict__ pair_list) {
+  __shared__ int base[kMaxExperts];
+  __shared__ int tot[kMaxExperts];
+  grid_dependents_launch();
+  grid_dependency_wait();  // the top-k launch's outputs
+  __shared__ int part[kMaxExperts][kScanSplit];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // per expert, kScanSplit threads each own a contiguous range of CTAs: their sums, an
+  // exclusive scan of those sums, then each range's prefixes written back in place
+  const int e_s = tid / kScanSplit, sub = tid % kScanSplit;
+  const int per = (nctas + kScanSplit - 1) / kScanSplit;
+  const int c_lo = sub * per, c_hi = min(nctas, c_lo + per);
+  if (e_s < E) {
+    int sum = 0;
+#pragma unroll 8
+    for (int c = c_lo; c < c_hi; ++c) sum += cta_hist[static_cast<size_t>(c) * E + e_s];
+    part[e_s][sub] = sum;
+  }
+  __syncthreads();
+  if (e_s < E) {
+    int run = 0;
+    for (int j = 0; j < sub; ++j) run += part[e_s][j];
+    if (sub == kScanSplit - 1) tot[e_s] = run + part[e_s][sub];
+#pragma unroll 8
+    for (int c = c_lo; c < c_hi; ++c) {
+      const int h = cta_hist[static_cast<size_t>(c) * E + e_s];
+      cta_hist[static_cast<size_t>(c) * E + e_s] = run;
+      run += h;
+    }
   }
   __syncthreads();
   if (warp == 0) {  // exclusive scan of the expert totals: lane owns 8 consecutive experts
@@ -133,7 +183,7 @@ __device__ __forceinline__ void group_pairs_block(const int32_t* __restrict__ to
     for (int j = 0; j < 8; ++j) {
       const int e = lane * 8 + j;
       local[j] = sum;
-      sum += e < E ? base[e] : 0;
+      sum += e < E ? tot[e] : 0;
     }
     int incl = sum;
 #pragma unroll
@@ -142,7 +192,6 @@ __device__ __forceinline__ void group_pairs_block(const int32_t* __restrict__ to
       if (lane >= off) incl += o;
     }
     const int excl = incl - sum;
-    __syncwarp();
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int e = lane * 8 + j;
@@ -154,50 +203,40 @@ __device__ __forceinline__ void group_pairs_block(const int32_t* __restrict__ to
     if (lane == 31) expert_offsets[E] = incl;
   }
   __syncthreads();
-  for (int r0 = p_lo; r0 < p_hi; r0 += 32) {
-    const int p = r0 + lane;
-    int e = p < p_hi ? __ldcg(topk_idx + p) : -1;
-    if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) e = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & lt_mask);
-    if (e >= 0) pair_list[base[e] + cnt[warp][e] + rank] = p;
-    __syncwarp();
-    if (e >= 0 && rank == 0) cnt[warp][e] += __popc(peers);
-    __syncwarp();
+  const int pairs_per_cta = kTopkWarps * k;
+  constexpr int kU = 4;  // pairs per thread per round, their loads issued together
+  for (int p0 = tid; p0 < P; p0 += kU * kGroupThreads) {
+    int e[kU], lr[kU], h[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int p = p0 + u * kGroupThreads;
+      e[u] = p < P ? topk_idx[p] : -1;
+      lr[u] = p < P ? local_rank[p] : 0;
+      if (static_cast<unsigned>(e[u]) >= static_cast<unsigned>(E)) e[u] = -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      h[u] = e[u] >= 0 ? cta_hist[static_cast<size_t>((p0 + u * kGroupThreads) / pairs_per_cta) * E + e[u]] : 0;
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (e[u] >= 0) pair_list[base[e[u]] + h[u] + lr[u]] = p0 + u * kGroupThreads;
   }
-}
-
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                              int32_t* __restrict__ topk_idx,
-                                                              float* __restrict__ topk_w,
-                                                              int32_t* __restrict__ expert_offsets,
-                                                              int32_t* __restrict__ pair_list,
-                                                              uint32_t* __restrict__ ticket) {
-  __shared__ int is_last;
-  grid_dependents_launch();  // the next launch may set up meanwhile; it waits for this one
-  grid_dependency_wait();    // logits, and the routing arrays an earlier launch may still read
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
-  if (t < T)
-    topk_softmax_warp(logits + static_cast<size_t>(t) * E, E, k, lane, topk_idx + static_cast<size_t>(t) * k,
-                      topk_w + static_cast<size_t>(t) * k);
-  __threadfence();  // this CTA's results are visible device-wide before its ticket is taken
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(ticket, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  group_pairs_block(topk_idx, T * k, E, expert_offsets, pair_list);
-  if (threadIdx.x == 0) *ticket = 0;  // ready for the next launch on this workspace
 }
 
 }  // namespace
 
 cudaError_t launch_route(const Dims& s, const float* logits, int32_t* topk_idx, float* topk_w,
-                         int32_t* expert_offsets, int32_t* pair_list, WsHeader* hdr, cudaStream_t st) {
-  const int grid = (s.T + kRouteWarps - 1) / kRouteWarps;
-  return launch_pdl(route_kernel, dim3(grid), dim3(kRouteThreads), 0, st, logits, s.T, s.E, s.k, topk_idx, topk_w,
-                    expert_offsets, pair_list, &hdr->route_ticket);
+                         int32_t* expert_offsets, int32_t* pair_list, void* workspace, cudaStream_t st) {
+  const int nctas = (s.T + kTopkWarps - 1) / kTopkWarps;
+  auto* base = static_cast<uint8_t*>(workspace);
+  auto* cta_hist = reinterpret_cast<int32_t*>(base + ws_route_offset(s));
+  auto* local_rank = reinterpret_cast<int32_t*>(base + ws_route_offset(s) + ws_route_hist_bytes(s));
+  cudaError_t err = launch_pdl(topk_kernel, dim3(nctas), dim3(kTopkWarps * 32), 0, st, logits, s.T, s.E, s.k,
+                               topk_idx, topk_w, cta_hist, local_rank);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(group_kernel, dim3(1), dim3(kGroupThreads), 0, st, static_cast<const int32_t*>(topk_idx),
+                    static_cast<int>(s.pairs()), s.E, s.k, nctas, cta_hist,
+                    static_cast<const int32_t*>(local_rank), expert_offsets, pair_list);
 }
 
 }  // namespace moe
