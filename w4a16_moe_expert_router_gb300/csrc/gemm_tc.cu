@@ -42,7 +42,7 @@
 //   warps 3-14  three dequant groups of four warps, one warp per TMEM lane
 //               quadrant; group G takes the stages t = G mod 3: each thread owns
 //               one GEMM row and writes the row's 64 weights of the stage into
-//               the stage's TMEM buffer (one tcgen05.st of 32 columns).  The
+//               the stage's TMEM buffer (two tcgen05.st of 16 columns).  The
 //               group that gets an item's last stage reads the row's two
 //               accumulators (tcgen05.ld, added in a fixed order) and runs the
 //               epilogue -- the gated GELU through a shared-memory exchange of
@@ -188,14 +188,12 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
 
@@ -569,28 +567,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // (scale, zero) of row m for the group(s) of this stage (every slot carries them)
       const int ngrp = max(groups_in_stage(s, a.p[pj].g), 1);
       const uint32_t* sz = reinterpret_cast<const uint32_t*>(st + kCodeOff - kSzBytes * ngrp);
-      {
-        const __half2 v0 = bits_h2(sz[m]);
-        const __half2 v1 = ngrp > 1 ? bits_h2(sz[kBlockRows + m]) : v0;
-        g0 = dq_group(__low2half2(v0), __high2half2(v0));
-        g1 = dq_group(__low2half2(v1), __high2half2(v1));
-      }
       // this row's 64 codes: two 16-byte halves, [half][row][16 B]; with groups of 32
       // the second half belongs to the stage's second group
       const uint4 c0 = *reinterpret_cast<const uint4*>(st + kCodeOff + m * 16);
       const uint4 c1 = *reinterpret_cast<const uint4*>(st + kCodeOff + kBlockRows * 16 + m * 16);
-      uint32_t w[32];
+      {
+        const __half2 v0 = bits_h2(sz[m]);
+        g0 = dq_group(__low2half2(v0), __high2half2(v0));
+        if (ngrp > 1) {
+          const __half2 v1 = bits_h2(sz[kBlockRows + m]);
+          g1 = dq_group(__low2half2(v1), __high2half2(v1));
+        } else {
+          g1 = g0;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&H.slot_empty[slot]));  // codes and scales are in registers
+      const int ast = t % kAStages;
+      uint32_t w[16];
       dequant_row8(c0.x, g0, w + 0);
       dequant_row8(c0.y, g0, w + 4);
       dequant_row8(c0.z, g0, w + 8);
       dequant_row8(c0.w, g0, w + 12);
-      dequant_row8(c1.x, g1, w + 16);
-      dequant_row8(c1.y, g1, w + 20);
-      dequant_row8(c1.z, g1, w + 24);
-      dequant_row8(c1.w, g1, w + 28);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&H.slot_empty[slot]));  // codes and scales are in registers
-      const int ast = t % kAStages;
       if (t >= kAStages) {
         // the TMEM stage is free once the MMAs of the stage that used it last (t - kAStages)
         // have completed: that stage's slot is released by the issuers' commits (and our arrivals)
@@ -599,7 +597,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (!ok) break;
       }
       tc_fence_after();
-      tc_st32(tmem + lane_bits + ast * kACols, w);
+      tc_st16(tmem + lane_bits + ast * kACols, w);
+      dequant_row8(c1.x, g1, w + 0);
+      dequant_row8(c1.y, g1, w + 4);
+      dequant_row8(c1.z, g1, w + 8);
+      dequant_row8(c1.w, g1, w + 12);
+      tc_st16(tmem + lane_bits + ast * kACols + 16, w);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
@@ -611,24 +614,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         ok = warp_wait(smem_addr(&H.d_full[b]), static_cast<uint32_t>(seq >> 1) & 1u, a, abort);
         if (!ok) break;
         tc_fence_after();
-        float acc[kNMax];
-        {
-          const uint32_t dcol = tmem + lane_bits + kDCol0 + b * kDCols;
-          // accumulator of k16 steps 0-1 plus that of steps 2-3, in this order
-#pragma unroll
-          for (int c = 0; c < kNMax; c += 16) {
-            uint32_t v0[16], v1[16];
-            tc_ld16(dcol + c, v0);
-            tc_ld16(dcol + kNMax + c, v1);
-            tc_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[c + i] = __uint_as_float(v0[i]) + __uint_as_float(v1[i]);
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&H.d_free[b]));  // the item after next may accumulate here
-        // ------------------------------------------------------------ epilogue
+        const uint32_t dcol = tmem + lane_bits + kDCol0 + b * kDCols;
+        // the accumulators in halves of 16 token columns (a half past the item's tokens is
+        // skipped: the MMA did not write it); each column is the accumulator of k16 steps
+        // 0-1 plus that of steps 2-3, in this order
         if (pj == 0) {
           // rows 0..63 gate j = 64*blk + m, rows 64..127 up j = 64*blk + m - 64; the up rows
           // reach the gate rows' threads through the exchange area of the item's accumulator
@@ -637,41 +626,63 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           // (seq >> 1)-th user of area seq & 1.
           float* xch = xch_all + b * 64 * kXchStride;
           const uint32_t xphase = static_cast<uint32_t>(seq >> 1) & 1u;
-          if (q >= 2) {
-            ok = warp_wait(smem_addr(&H.xch_done[b]), xphase ^ 1u, a, abort);  // previous reads finished
-            if (!ok) break;
-            float4* dst = reinterpret_cast<float4*>(xch + (m - 64) * kXchStride);
+          ok = q >= 2 ? warp_wait(smem_addr(&H.xch_done[b]), xphase ^ 1u, a, abort)  // previous reads finished
+                      : warp_wait(smem_addr(&H.xch_ready[b]), xphase, a, abort);
+          if (!ok) break;
+          const int j = 64 * blk + m;
+          for (int c = 0; c < kNMax && c < n_cnt; c += 16) {
+            uint32_t v0[16], v1[16];
+            tc_ld16(dcol + c, v0);
+            tc_ld16(dcol + kNMax + c, v1);
+            tc_wait_ld();
+            if (q >= 2) {
+              float4* dst = reinterpret_cast<float4*>(xch + (m - 64) * kXchStride + c);
 #pragma unroll
-            for (int i = 0; i < kNMax / 4; ++i)
-              dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&H.xch_ready[b]));
-          } else {
-            ok = warp_wait(smem_addr(&H.xch_ready[b]), xphase, a, abort);
-            if (!ok) break;
-            const float4* up4 = reinterpret_cast<const float4*>(xch + m * kXchStride);
-            const int j = 64 * blk + m;
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_float4(__uint_as_float(v0[4 * i]) + __uint_as_float(v1[4 * i]),
+                                     __uint_as_float(v0[4 * i + 1]) + __uint_as_float(v1[4 * i + 1]),
+                                     __uint_as_float(v0[4 * i + 2]) + __uint_as_float(v1[4 * i + 2]),
+                                     __uint_as_float(v0[4 * i + 3]) + __uint_as_float(v1[4 * i + 3]));
+            } else {
+              const float4* up4 = reinterpret_cast<const float4*>(xch + m * kXchStride + c);
 #pragma unroll
-            for (int i = 0; i < kNMax / 4; ++i) {
-              const float4 u = up4[i];
-              const float up[4] = {u.x, u.y, u.z, u.w};
+              for (int i = 0; i < 4; ++i) {
+                const float4 u = up4[i];
+                const float up[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const int n = 4 * i + c;
-                if (n < n_cnt)
-                  a.h[static_cast<size_t>(pos0 + n) * a.f + j] =
-                      __half_as_ushort(__float2half_rn(gelu(acc[n], a.act) * up[c]));
+                for (int cc = 0; cc < 4; ++cc) {
+                  const int n = c + 4 * i + cc;
+                  const float g = __uint_as_float(v0[4 * i + cc]) + __uint_as_float(v1[4 * i + cc]);
+                  if (n < n_cnt)
+                    a.h[static_cast<size_t>(pos0 + n) * a.f + j] =
+                        __half_as_ushort(__float2half_rn(gelu(g, a.act) * up[cc]));
+                }
               }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&H.xch_done[b]));
-            if (a.last == 1) sig_e = e;  // reported one stage later (see signal above)
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_addr(&H.d_free[b]));  // the item after next may accumulate here
+            mbar_arrive(smem_addr(q >= 2 ? &H.xch_ready[b] : &H.xch_done[b]));
+          }
+          if (q < 2 && a.last == 1) sig_e = e;  // reported one stage later (see signal above)
         } else {
           const int i_row = kBlockRows * blk + m;
+          for (int c = 0; c < kNMax && c < n_cnt; c += 16) {
+            uint32_t v0[16], v1[16];
+            tc_ld16(dcol + c, v0);
+            tc_ld16(dcol + kNMax + c, v1);
+            tc_wait_ld();
 #pragma unroll
-          for (int n = 0; n < kNMax; ++n)
-            if (n < n_cnt) a.y_out[static_cast<size_t>(a.pair_list[pos0 + n]) * a.d + i_row] = acc[n];
+            for (int i = 0; i < 16; ++i)
+              if (c + i < n_cnt)
+                a.y_out[static_cast<size_t>(a.pair_list[pos0 + c + i]) * a.d + i_row] =
+                    __uint_as_float(v0[i]) + __uint_as_float(v1[i]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&H.d_free[b]));  // the item after next may accumulate here
         }
       }
     }
