@@ -30,7 +30,7 @@ if ROOT not in sys.path:
 METRIC = "MoE expert-layer tokens/s at 256-token canvas; achieved HBM GB/s vs GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "expert_gemm_canvas256.txt")
-DOMINANT_SRC = os.path.join(ROOT, "w4a16_moe_expert_router_gb300", "csrc", "gemm_tc.cu")
+DOMINANT_SRC = os.path.join(ROOT, "w4a16_moe_expert_router_gb300", "csrc", "gemm_mma.cu")
 
 
 def log(*a):
@@ -351,8 +351,9 @@ def run_ours(args, rank, world, local):
         "hbm_frac_of_peak": layer_gbs / peak,
         "kernel_us": {"route": route_us, "experts": experts_us, "combine": comb_us},
         "roofline": {
-            "kernel": "expert_gemm_tc_kernel (gate_up + down grouped dequant GEMMs, one persistent tcgen05 "
-                      "launch; its timed segment also holds the expert-order row copy launched before it)",
+            "kernel": "expert_gemm_mma_kernel (gate_up + down grouped dequant GEMMs in one persistent launch: "
+                      "TMA/bulk-copy ring, in-register dequant, m16n8k16 tensor-core MMAs; its timed segment also "
+                      "holds the expert-order row copy launched before it)",
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "peak_source": peak_src, "traffic": profiled_traffic(),
             "algorithmic_bytes_per_launch": layer_bytes / layers,

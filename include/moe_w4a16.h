@@ -200,10 +200,11 @@ MOE_W4A16_API size_t moe_w4a16_prepared_bytes(const moe_w4a16_shape* shape, int3
  *   scale   fp16 bits [E][R][K/g]
  *   zero    fp16 bits [E][R][K/g]
  *   out     moe_w4a16_prepared_bytes(shape, which) bytes
- * The prepared layout is private to this library version: a stream of 64-column
- * stages per block of 128 GEMM rows, each stage holding the block's scale/zero
- * pairs for the groups that start in it followed by the codes in the order the
- * kernels' dequantiser consumes them.
+ * The prepared layout is private to this library version: per block of 128 GEMM
+ * rows, a stream of 128-column stages (the last of 64 columns when K is an odd
+ * multiple of 64), each split into eight strips of 16 rows, one per compute warp;
+ * a strip holds its rows' scale/zero pairs for the groups of the stage followed by
+ * the codes, each 32-bit word one m16n8k16 A fragment of one lane.
  * ERR_VALUE if a scale is not finite or |scale| > 32, or a zero-point lies outside
  * [0, 16] (the kernels' fp16 dequantisation is exact only in that range). */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_prepare(const moe_w4a16_shape* shape, int32_t which, const uint8_t* q,

@@ -140,35 +140,57 @@ def test_prepare_unprepare_round_trip(g1, g2, d, f, E):
         assert np.array_equal(q2, w[q]) and np.array_equal(s2, w[s]) and np.array_equal(z2, w[z])
 
 
+def _check_strip(seg, ng, steps, rows, codes, scale, zero, grp0, c0):
+    """One warp strip of one stage: (scale, zero) of rows (i, i + 8) per group, ordered
+    [i][group]; then words [kk // 4][lane][kk % 4] where nibble n of word (lane, kk)
+    holds strip row lane // 4 + 8 (n & 1), column c0 + 16 kk + 2 (lane % 4) + 8 ((n >> 1) & 1) + (n >> 2)."""
+    sz = seg[:64 * ng].view(np.uint16).reshape(8, ng, 2, 2)
+    for i in range(8):
+        for j in range(ng):
+            for h in range(2):
+                assert sz[i, j, h, 0] == scale[rows[i + 8 * h], grp0 + j]
+                assert sz[i, j, h, 1] == zero[rows[i + 8 * h], grp0 + j]
+    words = seg[64 * ng:64 * ng + steps * 128].view(np.uint32)
+    for kk in range(steps):
+        for lane in (0, 5, 17, 31):
+            gq, tq = lane // 4, lane % 4
+            wd = int(words[(kk // 4) * 128 + lane * 4 + kk % 4])
+            for n in range(8):
+                r = gq + 8 * (n & 1)
+                col = c0 + 16 * kk + 2 * tq + 8 * ((n >> 1) & 1) + (n >> 2)
+                assert (wd >> (4 * n)) & 15 == codes[rows[r], col]
+
+
 def test_prepared_word_layout_matches_documented_order():
-    """First stage of block 0 of expert 0 of gate_up: (scale, zero) of 128 GEMM rows,
-    then words [half][GEMM row][4]; GEMM row r is gate row r (r < 64) or up row
-    f + r - 64; nibble i of word w holds column 32*half + 8w + (0,2,4,6,1,3,5,7)[i]."""
-    wl = synth.WORKLOADS["tiny"]
+    """Stages of 128 columns (the last of 64 when K is an odd multiple of 64); per
+    stage, eight warp strips of 16 GEMM rows; gate_up strip w of block b holds gate
+    rows 64b + 8w + (0..7) and the matching up rows f + 64b + 8w + (0..7), down strip
+    w of block b holds rows 128b + 16w + (0..15)."""
+    wl = synth.Workload("t", 4, 256, 192, 1, 1, 64, 64)   # d = 256 (2 stages), f = 192 (128 + 64)
     w = synth.make_weights(wl, seed=9)
     sh = runtime.shape_of(wl)
-    prep = B.moe_w4a16_prepare(sh, B.GATE_UP, w["gate_up_q"], w["gate_up_scale"], w["gate_up_zero"])
-    codes = B.moe_w4a16_unpack(w["gate_up_q"])[0]          # [2f][d]
     f = wl.inter
-    row = lambda r: r if r < 64 else f + r - 64
-    sz = prep[:512].view(np.uint16).reshape(128, 2)
-    for r in range(128):
-        assert sz[r, 0] == w["gate_up_scale"][0, row(r), 0]
-        assert sz[r, 1] == w["gate_up_zero"][0, row(r), 0]
-    words = prep[512:512 + 4096].view(np.uint32).reshape(2, 128, 4)
-    order = (0, 2, 4, 6, 1, 3, 5, 7)
-    for hf in (0, 1):
-        for r in (0, 5, 63, 64, 127):
-            for wi in (0, 3):
-                c0 = 32 * hf + 8 * wi
-                wd = int(words[hf, r, wi])
-                assert [(wd >> (4 * i)) & 15 for i in range(8)] == [codes[row(r), c0 + order[i]] for i in range(8)]
-    # the second stage of the down projection starts after the first stage's 512 + 4096 bytes
+    gu = B.moe_w4a16_prepare(sh, B.GATE_UP, w["gate_up_q"], w["gate_up_scale"], w["gate_up_zero"])
+    codes = B.moe_w4a16_unpack(w["gate_up_q"])[0]          # [2f][d]
+    sc, ze = w["gate_up_scale"][0], w["gate_up_zero"][0]
+    strip = 8 * 128 + 2 * 64                                # one warp's part of a full stage, groups of 64
+    block = 2 * 8 * strip                                   # K = 256: two full stages
+    for b, st, wv in ((0, 0, 0), (0, 1, 3), (2, 1, 7)):
+        rows = [64 * b + 8 * wv + r if r < 8 else f + 64 * b + 8 * wv + r - 8 for r in range(16)]
+        off = b * block + st * 8 * strip + wv * strip
+        _check_strip(gu[off:off + strip], 2, 8, rows, codes, sc, ze, 2 * st, 128 * st)
     dn = B.moe_w4a16_prepare(sh, B.DOWN, w["down_q"], w["down_scale"], w["down_zero"])
     dcodes = B.moe_w4a16_unpack(w["down_q"])[0]             # [d][f]
-    words2 = dn[2 * (512 + 4096) - 4096: 2 * (512 + 4096)].view(np.uint32).reshape(2, 128, 4)
-    wd = int(words2[1, 7, 1])
-    assert [(wd >> (4 * i)) & 15 for i in range(8)] == [dcodes[7, 64 + 32 + 8 + order[i]] for i in range(8)]
+    sc, ze = w["down_scale"][0], w["down_zero"][0]
+    tail = 4 * 128 + 64                                     # one warp's part of the last 64 columns
+    dblock = 8 * strip + 8 * tail
+    for b, wv in ((0, 2), (1, 6)):
+        rows = [128 * b + 16 * wv + r for r in range(16)]
+        off = b * dblock + wv * strip
+        _check_strip(dn[off:off + strip], 2, 8, rows, dcodes, sc, ze, 0, 0)
+        off = b * dblock + 8 * strip + wv * tail
+        _check_strip(dn[off:off + tail], 1, 4, rows, dcodes, sc, ze, 2, 128)
+    assert dn.nbytes == 2 * dblock
 
 
 def test_prepare_rejects_out_of_range_scale_and_zero():

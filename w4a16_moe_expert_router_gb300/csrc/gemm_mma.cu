@@ -1,0 +1,647 @@
+// gemm_mma.cu -- grouped W4A16 expert GEMMs with the weights dequantised in
+// registers and multiplied on the warp-level tensor-core path.
+//
+// Model card "srswti/axe-diffusion-ksl-xe", "the kernels we built": the GEMM
+// reads packed nibbles and dequantises inline, so HBM carries real 4-bit
+// traffic; one launch covers all experts; the activation is folded into the
+// first GEMM's epilogue.  One persistent launch runs both projections:
+//   gate_up:  a[p][n] = sum_k Wgu[e][n][k] x[t(p)][k]
+//             h[pos(p)][j] = gelu(a[p][j]) * a[p][f+j]  -> fp16, rows in expert-sorted order
+//   down:     y[p][i] = sum_j Wd[e][i][j] h[pos(p)][j]   -> fp32, rows by pair id p = t*k + r
+// The work list holds every gate_up item followed by every down item; an item
+// is (projection, expert, 128-row block, chunk of <= 32 tokens) over the whole
+// contraction.  A down item of expert e starts once all gate_up items of e have
+// written their h rows (a per-expert counter, bounded wait).
+//
+// Why registers and mma.sync: a canvas gives an expert ~16 tokens, so each
+// weight is used by few MACs and the work is the dequantisation, not the
+// multiply.  A thread turns one 32-bit word of codes into exactly the four f16x2
+// registers of an m16n8k16 A fragment and hands them to the MMA itself; no
+// weight tile is written to shared or tensor memory and no other warp has to be
+// told that it is ready.  The tokens (the B operand) are shared by the CTA's
+// eight compute warps through a TMA-filled shared-memory ring.
+//
+// Arithmetic: the zero-point is split into its nearest integer zr and the rest
+// zf = z - zr, and each weight is formed as w = fp16((q - zr) * s - fp16(zf * s)):
+// q - zr is exact in fp16 and the fused multiply-add rounds once.  The MMA
+// multiplies w with the fp16 activations into fp32 accumulators (16-column
+// steps in contraction order).
+//
+// Roles of the persistent CTA (two per SM; a stage is 128 contraction columns,
+// the last one 64 when the contraction is an odd multiple of 64):
+//   warp 0      producer: claims items one ahead of use, publishes each in a
+//               small queue in shared memory, and per stage issues one bulk
+//               copy of the stage's weight segment (codes and (scale, zero)
+//               pairs of all eight warps, contiguous in the stream) and two 2-D
+//               TMA loads (64 columns x 32 token rows each, 128-byte swizzle)
+//               of the activations into the same slot of a ring of five;
+//   warps 1-8   compute: warp w owns 16 GEMM rows of the block (for gate_up 8
+//               gate rows and the 8 matching up rows, so the gated GELU needs
+//               nothing from another warp).  Per stage each reads its rows'
+//               codes (16-byte vectors, 512 contiguous bytes per warp) and
+//               (scale, zero) pairs from the slot, dequantises them into A
+//               fragments, reads the token fragments with ldmatrix and issues
+//               the MMAs; an item's accumulators stay in registers.  The
+//               kernel is specialised per item on the token tiles (1-4 tiles
+//               of 8) and the group size, so a stage has no data-dependent
+//               branches.
+// Every wait is bounded: on expiry the CTA records MOE_W4A16_ERR_TIMEOUT in the
+// workspace and all roles leave their loops; the producer drains its copies.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMmaWarps = kBlockRows / kStripRows;  // compute warps, one 16-row strip each
+constexpr int kThreads = (1 + kMmaWarps) * 32;     // 288
+constexpr int kCtasPerSm = 2;
+constexpr int kSlots = 5;                          // stages in flight per CTA
+constexpr int kQueue = 4;                          // item descriptors in flight per CTA
+constexpr int kBBoxRows = 32;                      // TMA box: 64 columns x 32 token rows
+constexpr int kBoxBytes = kBBoxRows * 128;         // 4 KiB, 128-byte swizzle
+constexpr int kBBytes = 2 * kBoxBytes;             // a stage's token tile: two boxes
+constexpr int kSzBytesW = 64;                      // one warp's (scale, zero) pairs of one group
+constexpr int kWMaxBytes = kMmaWarps * (1024 + 4 * kSzBytesW);  // a stage's weights, at most 10 KiB
+constexpr int kSlotBytes = 18432;                  // [tokens 8 KiB][weights <= 10 KiB], a multiple of 1024
+static_assert(kBBytes + kWMaxBytes <= kSlotBytes && kSlotBytes % 1024 == 0, "slot layout");
+constexpr int kHeaderBytes = 4096;
+constexpr int kSmemBytes = 1024 + kHeaderBytes + kSlots * kSlotBytes;  // +1024 for alignment
+
+struct Proj {
+  const uint8_t* w;         // prepared stream of the projection, all experts
+  int64_t expert_bytes;     // stream bytes per expert
+  int64_t block_bytes;      // stream bytes per 128-row block
+  int nblocks;              // blocks per expert
+  int K;                    // contraction length (multiple of 64)
+  int g;                    // quantisation group along K (32, 64 or 128)
+};
+
+struct MmArgs {
+  Proj p[2];                // 0: gate_up, 1: down
+  int first, last;          // projections in this launch's work list (0 <= first <= last <= 1)
+  const int32_t* offsets;   // [E+1]
+  const int32_t* pair_list; // [T*k]
+  int E;
+  uint16_t* h;              // gate_up output, down input [T*k][f] (expert-sorted rows)
+  float* y_out;             // down output [T*k][d]
+  int f, d, act;
+  int32_t* err;
+  int32_t* counter;         // work counter of this launch
+  int32_t* done_ctas;       // CTAs that have finished; the last one resets both counters
+  int32_t* gu_done;         // [E] gate_up warps finished per expert (kMmaWarps per item)
+};
+
+// Shared-memory header (at the 1024-aligned base of dynamic shared memory).
+struct __align__(8) MmHeader {
+  uint64_t slot_full[kSlots];   // the stage's tokens and weights landed
+  uint64_t slot_empty[kSlots];  // the compute warps have read the stage
+  uint64_t item_full[kQueue];   // queue entry written
+  uint64_t item_empty[kQueue];  // the compute warps are done with the item
+  int item_desc[kQueue][3];     // {proj | tokens << 8 | block << 16 (or -1 at the end), expert, first row}
+  int abort;
+  int prefix[2][kMaxExperts + 1];  // items of each projection before expert e
+  int offs[kMaxExperts + 1];    // expert_offsets, copied once
+};
+static_assert(sizeof(MmHeader) <= kHeaderBytes, "header fits");
+
+// Weight bytes of one stage of kk16 16-column steps (all eight warps) with groups of g.
+__device__ __forceinline__ uint32_t stage_weight_bytes(int kk16, int g) {
+  const int ng = (16 * kk16) / min(g, 16 * kk16);
+  return static_cast<uint32_t>(kMmaWarps * (kk16 * 128 + kSzBytesW * ng));
+}
+
+__device__ __forceinline__ int expert_of(int item, const int* prefix, int E) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {  // largest e with prefix[e] <= item
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= item) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Work item of one projection -> (expert, 128-row block, token chunk); the chunk
+// varies fastest, so concurrent items of a busy expert share weight blocks in L2.
+__device__ __forceinline__ void decode_item(int item, const int* prefix, const int* offs, int E, int& expert,
+                                            int& blk, int& n_cnt, int& pos0) {
+  const int e = expert_of(item, prefix, E);
+  const int n_e = offs[e + 1] - offs[e];
+  const int nch = (n_e + kChunkN - 1) / kChunkN;
+  const int r = item - prefix[e];
+  const int c = r % nch;
+  expert = e;
+  blk = r / nch;
+  n_cnt = min(kChunkN, n_e - kChunkN * c);
+  pos0 = offs[e] + kChunkN * c;
+}
+
+constexpr uint64_t kDepWaitNs = 2000000000ull;  // bound of the wait for an expert's gate_up outputs
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Dequantiser constants of one thread's two rows (g and g+8 of its warp's 16)
+// for one group, each broadcast to both halves of an f16x2: the zero-point split
+// into its nearest integer zr and the rest zf = z - zr, so that
+// (q - zr) * s - zf * s = (q - z) * s.
+struct DqRows {
+  __half2 zb_lo;  // 1024 + zr of row g (exact)
+  __half2 s_lo;
+  __half2 c_lo;   // -fp16(zf * s) of row g
+  __half2 zb_hi;  // 64 + zr of row g + 8 (exact)
+  __half2 s_hi;
+  __half2 c_hi;
+};
+// v.x = (scale, zero) of row g, v.y = those of row g + 8 (fp16 pairs).  For
+// 0 <= z <= 16, fp16(z + 1024) is 1024 + zr with zr = z rounded to the nearest
+// integer (ties to even): fp16 has unit spacing in [1024, 2048).
+__device__ __forceinline__ DqRows dq_rows(uint32_t vx, uint32_t vy) {
+  const uint32_t zz = __byte_perm(vx, vy, 0x7632), ss = __byte_perm(vx, vy, 0x5410);
+  const __half2 z = bits_h2(zz), s = bits_h2(ss);
+  const __half2 zb1 = __hadd2(z, bits_h2(0x64006400u));            // 1024 + zr, both rows
+  const __half2 zr = __hsub2(zb1, bits_h2(0x64006400u));
+  const __half2 c = __hneg2(__hmul2(__hsub2(z, zr), s));
+  const __half2 zb = __hsub2(zb1, bits_h2(0x63800000u));           // (1024 + zr_g, 64 + zr_g8)
+  DqRows k;
+  k.zb_lo = __low2half2(zb);
+  k.s_lo = __low2half2(s);
+  k.c_lo = __low2half2(c);
+  k.zb_hi = __high2half2(zb);
+  k.s_hi = __high2half2(s);
+  k.c_hi = __high2half2(c);
+  return k;
+}
+
+// One word of codes -> the m16n8k16 A fragment of the thread: nibbles (0,4) are
+// row g columns (2t, 2t+1), (1,5) row g+8 columns (2t, 2t+1), (2,6) row g
+// columns (2t+8, 2t+9), (3,7) row g+8 columns (2t+8, 2t+9).  (1024 + q) and
+// (64 + q) come from OR-ing exponent bits onto the nibbles; one fp16 subtract of
+// (1024 + zr) or (64 + zr) gives q - zr exactly, and one fused multiply-add
+// rounds the weight once.
+__device__ __forceinline__ void dequant_frag(uint32_t w, const DqRows& k, uint32_t (&a)[4]) {
+  const uint32_t w8 = w >> 8;
+  a[0] = h2_bits(__hfma2(__hsub2(bits_h2(and_or(w, 0x000f000fu, 0x64006400u)), k.zb_lo), k.s_lo, k.c_lo));
+  a[1] = h2_bits(__hfma2(__hsub2(bits_h2(and_or(w, 0x00f000f0u, 0x54005400u)), k.zb_hi), k.s_hi, k.c_hi));
+  a[2] = h2_bits(__hfma2(__hsub2(bits_h2(and_or(w8, 0x000f000fu, 0x64006400u)), k.zb_lo), k.s_lo, k.c_lo));
+  a[3] = h2_bits(__hfma2(__hsub2(bits_h2(and_or(w8, 0x00f000f0u, 0x54005400u)), k.zb_hi), k.s_hi, k.c_hi));
+}
+
+__device__ __forceinline__ float gelu(float a, int act) {
+  if (act == 1) return 0.5f * a * (1.f + erff(a * 0.70710678118654752f));
+  return 0.5f * a * (1.f + tanhf(0.79788456080286536f * (a + 0.044715f * a * a * a)));
+}
+
+// Warp-uniform bounded wait: every lane polls the barrier (so each acquires the
+// phase), the warp leaves together once all lanes have seen it complete, and the
+// decision to give up is lane 0's, broadcast.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const MmArgs& a, volatile int* abort) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSuspendNs))) return true;
+    int give_up = 0;
+    if ((threadIdx.x & 31) == 0) {
+      give_up = *abort != 0;
+      if (!give_up && global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicExch(a.err, kStatusTimeout);
+        *abort = 1;
+        give_up = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+  }
+}
+
+// Work item as the compute warps read it from the queue.
+struct ItemView {
+  int pj, n_cnt, blk, e, pos0, g;
+};
+
+__device__ __forceinline__ bool read_item(const MmHeader& H, int i, const MmArgs& a, ItemView& v) {
+  const int d0 = H.item_desc[i % kQueue][0];
+  if (d0 < 0) return false;
+  v.pj = d0 & 1;
+  v.n_cnt = (d0 >> 8) & 0xff;
+  v.blk = d0 >> 16;
+  v.e = H.item_desc[i % kQueue][1];
+  v.pos0 = H.item_desc[i % kQueue][2];
+  v.g = a.p[v.pj].g;
+  return true;
+}
+
+// One stage of one compute warp: KK 16-column steps, NT tiles of 8 tokens, groups of G.
+template <int NT, int G, int KK>
+__device__ __forceinline__ bool run_stage(const MmArgs& a, MmHeader& H, volatile int* abort, float (&acc)[NT][4],
+                                          int& slot, uint32_t& phase, uint32_t ring_s, const uint32_t (&loff)[4],
+                                          int sw, int lane) {
+  constexpr int NG = (16 * KK) / (G < 16 * KK ? G : 16 * KK);  // groups in the stage
+  constexpr int kStepsPerGroup = KK / NG;
+  if (!warp_wait(smem_addr(&H.slot_full[slot]), phase, a, abort)) return false;
+  const uint32_t sl = ring_s + slot * kSlotBytes;
+  // this warp's part of the stage's weights: [(scale, zero) x NG][codes]
+  const uint32_t wseg = sl + kBBytes + sw * (KK * 128 + kSzBytesW * NG);
+  uint32_t words[KK];
+#pragma unroll
+  for (int q = 0; q < KK / 4; ++q)
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(words[4 * q]), "=r"(words[4 * q + 1]), "=r"(words[4 * q + 2]), "=r"(words[4 * q + 3])
+                 : "r"(wseg + kSzBytesW * NG + q * 512 + lane * 16));
+  uint32_t szw[2 * NG];
+  const uint32_t szaddr = wseg + (lane >> 2) * (8 * NG);
+  if (NG == 1) {
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(szw[0]), "=r"(szw[1]) : "r"(szaddr));
+  } else {
+#pragma unroll
+    for (int q = 0; q < NG / 2; ++q)
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(szw[4 * q]), "=r"(szw[4 * q + 1]), "=r"(szw[4 * q + 2]), "=r"(szw[4 * q + 3])
+                   : "r"(szaddr + 16 * q));
+  }
+  DqRows k;
+#pragma unroll
+  for (int kk = 0; kk < KK; ++kk) {
+    if (kk % kStepsPerGroup == 0) k = dq_rows(szw[2 * (kk / kStepsPerGroup)], szw[2 * (kk / kStepsPerGroup) + 1]);
+    uint32_t af[4];
+    dequant_frag(words[kk], k, af);
+    uint32_t b[4][2];
+    const uint32_t baddr = sl + (kk / 4) * kBoxBytes + loff[kk % 4];
+    ldmatrix_x4(baddr, b[0][0], b[0][1], b[1][0], b[1][1]);
+    if (NT > 2) ldmatrix_x4(baddr + 16 * 128, b[2][0], b[2][1], b[3][0], b[3][1]);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mma_f16_16816(acc[nt], af, b[nt][0], b[nt][1]);
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_addr(&H.slot_empty[slot]));  // shared-memory reads of the stage done
+  if (++slot == kSlots) {
+    slot = 0;
+    phase ^= 1u;
+  }
+  return true;
+}
+
+// One item of one compute warp: every stage of the contraction, then the epilogue.
+// Returns false if a wait gave up.
+template <int NT, int G>
+__device__ __forceinline__ bool run_item(const MmArgs& a, MmHeader& H, volatile int* abort, const ItemView& v,
+                                         int& slot, uint32_t& phase, uint32_t ring_s, const uint32_t (&loff)[4],
+                                         int sw, int lane) {
+  const int gq = lane >> 2, tq = lane & 3;
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[nt][j] = 0.f;
+  const int K = a.p[v.pj].K;
+  for (int c0 = 0; c0 + kStageCols <= K; c0 += kStageCols)
+    if (!run_stage<NT, G, 8>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
+  if (G < 128 && (K % kStageCols) != 0)  // the last 64 columns
+    if (!run_stage<NT, (G < 64 ? G : 64), 4>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
+  // ------------------------------------------------------------------ epilogue
+  if (v.pj == 0) {
+    // rows gq: gate j, gq + 8: up j, with j = 64 * blk + 8 * sw + gq
+    const int j = 64 * v.blk + 8 * sw + gq;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = 8 * nt + 2 * tq;
+      if (n < v.n_cnt)
+        a.h[static_cast<size_t>(v.pos0 + n) * a.f + j] =
+            __half_as_ushort(__float2half_rn(gelu(acc[nt][0], a.act) * acc[nt][2]));
+      if (n + 1 < v.n_cnt)
+        a.h[static_cast<size_t>(v.pos0 + n + 1) * a.f + j] =
+            __half_as_ushort(__float2half_rn(gelu(acc[nt][1], a.act) * acc[nt][3]));
+    }
+    if (a.last == 1) {
+      // report the h rows to the expert's counter: __syncwarp orders the lanes' stores before
+      // lane 0's release, which is cumulative at device scope
+      __syncwarp();
+      if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a.gu_done + v.e) : "memory");
+    }
+  } else {
+    const int i_row = kBlockRows * v.blk + 16 * sw + gq;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = 8 * nt + 2 * tq;
+      if (n < v.n_cnt) {
+        float* yr = a.y_out + static_cast<size_t>(a.pair_list[v.pos0 + n]) * a.d + i_row;
+        yr[0] = acc[nt][0];
+        yr[8] = acc[nt][2];
+      }
+      if (n + 1 < v.n_cnt) {
+        float* yr = a.y_out + static_cast<size_t>(a.pair_list[v.pos0 + n + 1]) * a.d + i_row;
+        yr[0] = acc[nt][1];
+        yr[8] = acc[nt][3];
+      }
+    }
+  }
+  return true;
+}
+
+template <int G>
+__device__ __forceinline__ bool run_item_g(const MmArgs& a, MmHeader& H, volatile int* abort, const ItemView& v,
+                                           int& slot, uint32_t& phase, uint32_t ring_s, const uint32_t (&loff)[4],
+                                           int sw, int lane) {
+  switch ((v.n_cnt + 7) / 8) {
+    case 1: return run_item<1, G>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+    case 2: return run_item<2, G>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+    case 3: return run_item<3, G>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+    default: return run_item<4, G>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    expert_gemm_mma_kernel(const MmArgs a, const __grid_constant__ CUtensorMap map_x,
+                           const __grid_constant__ CUtensorMap map_h) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  MmHeader& H = *reinterpret_cast<MmHeader*>(smem);
+  uint8_t* ring = smem + kHeaderBytes;
+  volatile int* abort = &H.abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_addr(&H.slot_full[i]), 1);
+      mbar_init(smem_addr(&H.slot_empty[i]), kMmaWarps);
+    }
+    for (int i = 0; i < kQueue; ++i) {
+      mbar_init(smem_addr(&H.item_full[i]), 1);
+      mbar_init(smem_addr(&H.item_empty[i]), kMmaWarps);
+    }
+    H.abort = 0;
+    fence_barrier_init();
+  }
+  // everything above is set-up; the routing arrays, the row copy and h come from earlier launches
+  grid_dependents_launch();
+  grid_dependency_wait();
+  if (warp == 1) {  // items per expert = blocks * ceil(n_e / 32); exclusive scans, 8 experts per lane
+    for (int pj = 0; pj < 2; ++pj) {
+      const int nb = a.p[pj].nblocks;
+      int loc[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int e = lane * 8 + j;
+        loc[j] = sum;
+        if (e < a.E) sum += nb * ((a.offsets[e + 1] - a.offsets[e] + kChunkN - 1) / kChunkN);
+      }
+      int incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (lane * 8 + j < a.E) H.prefix[pj][lane * 8 + j] = incl - sum + loc[j];
+      if (lane == 31) H.prefix[pj][a.E] = incl;
+    }
+    for (int e = lane; e <= a.E; e += 32) H.offs[e] = a.offsets[e];
+  }
+  __syncthreads();
+  // the launch's work list: [gate_up items][down items], restricted to projections first..last
+  const int total0 = a.first == 0 ? H.prefix[0][a.E] : 0;
+  const int total = total0 + (a.last == 1 ? H.prefix[1][a.E] : 0);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    // (the whole warp waits, lane 0 writes and issues)
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&map_x) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&map_h) : "memory");
+    }
+    // every weight byte is read once: it leaves L2 first, so that h, y and the token rows stay
+    const uint64_t w_policy = l2_evict_first_policy();
+    uint32_t issued_mask = 0;  // slots whose last phase carried copies
+    uint32_t issued_par = 0;   // parity of that phase, one bit per slot
+    bool ok = true;
+    int t = 0;
+    int next = 0;
+    if (lane == 0) next = atomicAdd(a.counter, 1);  // claimed one item ahead
+    for (int i = 0; ok; ++i) {
+      const int item = __shfl_sync(0xffffffffu, next, 0);
+      const bool done = item >= total;
+      if (lane == 0 && !done) next = atomicAdd(a.counter, 1);
+      const int pj = (a.first == 0 && item < total0) ? 0 : 1;
+      int e = 0, blk = 0, n_cnt = 0, pos0 = 0;
+      if (!done) decode_item(pj == 0 ? item : item - total0, H.prefix[pj], H.offs, a.E, e, blk, n_cnt, pos0);
+      ok = warp_wait(smem_addr(&H.item_empty[i % kQueue]), ((i / kQueue) & 1) ^ 1, a, abort);
+      if (!ok) break;
+      if (lane == 0) {
+        H.item_desc[i % kQueue][0] = done ? -1 : (pj | (n_cnt << 8) | (blk << 16));
+        H.item_desc[i % kQueue][1] = e;
+        H.item_desc[i % kQueue][2] = pos0;
+        mbar_arrive(smem_addr(&H.item_full[i % kQueue]));  // release: the entry is visible to its waiters
+      }
+      __syncwarp();
+      if (done) break;
+      if (pj == 1 && a.first == 0) {
+        // a down item reads the h rows of its expert: wait until every gate_up warp of the
+        // expert has written them
+        if (lane == 0) {
+          const int need = kMmaWarps * a.p[0].nblocks * ((H.offs[e + 1] - H.offs[e] + kChunkN - 1) / kChunkN);
+          const uint64_t t0 = global_timer_ns();
+          for (;;) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.gu_done + e) : "memory");
+            if (v >= need) break;
+            if (*abort || global_timer_ns() - t0 > kDepWaitNs) {
+              atomicExch(a.err, kStatusTimeout);
+              *abort = 1;
+              ok = false;
+              break;
+            }
+            __nanosleep(256);
+          }
+          // the TMA loads below read those rows through the async proxy
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      const Proj& P = a.p[pj];
+      const CUtensorMap* bmap = pj == 0 ? &map_x : &map_h;
+      const uint8_t* wsrc = P.w + static_cast<int64_t>(e) * P.expert_bytes + static_cast<int64_t>(blk) * P.block_bytes;
+      for (int c0 = 0; c0 < P.K; c0 += kStageCols, ++t) {
+        const int slot = t % kSlots;
+        const uint32_t par = static_cast<uint32_t>(t / kSlots) & 1u;
+        ok = warp_wait(smem_addr(&H.slot_empty[slot]), par ^ 1u, a, abort);
+        if (!ok) break;
+        const int kk16 = min(kStageCols, P.K - c0) / 16;  // 8, or 4 for a last 64-column stage
+        const uint32_t wbytes = stage_weight_bytes(kk16, P.g);
+        if (lane == 0) {
+          const uint32_t full = smem_addr(&H.slot_full[slot]);
+          const uint32_t dst = smem_addr(ring + slot * kSlotBytes);
+          mbar_arrive_expect_tx(full, (kk16 / 4) * kBoxBytes + wbytes);
+          bulk_g2s_hint(dst + kBBytes, wsrc, wbytes, full, w_policy);
+          tma_load_2d(dst, bmap, c0, pos0, full);
+          if (kk16 == 8) tma_load_2d(dst + kBoxBytes, bmap, c0 + 64, pos0, full);
+        }
+        __syncwarp();
+        wsrc += wbytes;
+        issued_mask |= 1u << slot;
+        issued_par = (issued_par & ~(1u << slot)) | (par << slot);
+      }
+    }
+    // drain: every copy issued has landed before the CTA can exit
+    if (lane == 0)
+      for (int i = 0; i < kSlots; ++i)
+        if ((issued_mask >> i) & 1u) mbar_wait(smem_addr(&H.slot_full[i]), (issued_par >> i) & 1u, a.err);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ compute warps
+    const int sw = warp - 1;  // the warp's 16 rows of the block
+    // ldmatrix: lanes 0-7 / 8-15 / 16-23 / 24-31 address token rows 0-7 / 0-7 / 8-15 / 8-15 at the
+    // step's first / second / first / second 8 columns; the token tile is 128-byte swizzled (the
+    // 16-byte chunk c of token row n sits at chunk c ^ (n & 7))
+    uint32_t loff[4];
+    {
+      const int lrow = ((lane >> 4) << 3) + (lane & 7), lhi = (lane >> 3) & 1;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) loff[kk] = lrow * 128 + ((((2 * kk + lhi) ^ (lrow & 7))) << 4);
+    }
+    const uint32_t ring_s = smem_addr(ring);
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int i = 0;; ++i) {
+      if (!warp_wait(smem_addr(&H.item_full[i % kQueue]), (i / kQueue) & 1, a, abort)) break;
+      ItemView v;
+      if (!read_item(H, i, a, v)) break;
+      const bool ok = v.g == 32   ? run_item_g<32>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
+                      : v.g == 64 ? run_item_g<64>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
+                                  : run_item_g<128>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&H.item_empty[i % kQueue]));
+    }
+  }
+  __syncthreads();
+  // The last CTA to finish clears the work counter for the next launch on this
+  // workspace: by then every CTA has seen the list exhausted and claims no more.
+  if (tid == 0 && atomicAdd(a.done_ctas, 1) == static_cast<int>(gridDim.x) - 1) {
+    *a.counter = 0;
+    *a.done_ctas = 0;
+  }
+}
+
+// Token rows of every (token, expert) pair, copied in expert-sorted order:
+// xs[pos] = x[pair_list[pos] / k].  One warp per row, 16-byte accesses.  Also
+// clears the per-expert gate_up counters that the GEMM launch after it counts up.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ pair_list, int P, int k, int d,
+                                                          uint16_t* __restrict__ xs, int32_t* __restrict__ gu_done,
+                                                          int E) {
+  grid_dependents_launch();
+  grid_dependency_wait();  // pair_list of the routing launch
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) gu_done[e] = 0;
+  const int pos = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (pos >= P) return;
+  const int t = pair_list[pos] / k;
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
+  uint4* dst = reinterpret_cast<uint4*>(xs + static_cast<size_t>(pos) * d);
+  // up to 8 loads in flight per lane before the first store (d <= 8192: 32 per lane)
+  for (int i0 = 0; i0 < d / 8; i0 += 32 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * 32 + lane;
+      if (i < d / 8) v[j] = src[i];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * 32 + lane;
+      if (i < d / 8) dst[i] = v[j];
+    }
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// 2-D tensor map over rows x cols fp16 (row-major), box 64 columns x 32 rows, 128-byte swizzle.
+bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {kBoxCols, kBBoxRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t init_gemm_kernels(int* blocks_per_sm) {
+  const void* fn = reinterpret_cast<const void*>(expert_gemm_mma_kernel);
+  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (err != cudaSuccess) return err;
+  *blocks_per_sm = kCtasPerSm;
+  return cudaSuccess;
+}
+
+cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, const int32_t* expert_offsets,
+                               const int32_t* pair_list, const uint8_t* w_gate_up, const uint8_t* w_down,
+                               const GemmWorkspace& ws, int grid, cudaStream_t st) {
+  const int P = static_cast<int>(s.pairs());
+  MmArgs a{};
+  const int K[2] = {s.d, s.f}, g[2] = {s.g1, s.g2}, nb[2] = {s.f / 64, s.d / kBlockRows};
+  const uint8_t* w[2] = {w_gate_up, w_down};
+  for (int pj = 0; pj < 2; ++pj) {
+    a.p[pj].w = w[pj];
+    a.p[pj].K = K[pj];
+    a.p[pj].g = g[pj];
+    a.p[pj].nblocks = nb[pj];
+    a.p[pj].block_bytes = int64_t(kBlockRows) * K[pj] / 2 + int64_t(kBlockRows) * (K[pj] / g[pj]) * 4;
+    a.p[pj].expert_bytes = a.p[pj].block_bytes * nb[pj];
+  }
+  a.first = (which & kGemmGateUp) ? 0 : 1;
+  a.last = (which & kGemmDown) ? 1 : 0;
+  if (which == 0 || a.first > a.last) return cudaErrorInvalidValue;
+  a.offsets = expert_offsets;
+  a.pair_list = pair_list;
+  a.E = s.E;
+  a.f = s.f;
+  a.d = s.d;
+  a.act = s.act;
+  a.err = &ws.hdr->error;
+  a.h = ws.h;
+  a.y_out = ws.y;
+  // gate_up launches (alone or fused) and down-only launches keep separate counters
+  const int c = a.first == 0 ? 0 : 1;
+  a.counter = &ws.hdr->next_item[c];
+  a.done_ctas = &ws.hdr->done_ctas[c];
+  a.gu_done = ws.gu_done;
+  if (which & kGemmGateUp) {
+    // the token rows are first copied in expert order
+    cudaError_t err = launch_pdl(gather_rows_kernel, dim3((P + 7) / 8), dim3(256), 0, st, x, pair_list, P, s.k, s.d,
+                                 ws.xs, ws.gu_done, s.E);
+    if (err != cudaSuccess) return err;
+  }
+  CUtensorMap map_x, map_h;
+  if (!make_row_map(&map_x, ws.xs, P, s.d) || !make_row_map(&map_h, ws.h, P, s.f)) return cudaErrorInvalidValue;
+  return launch_pdl(expert_gemm_mma_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, a, map_x, map_h);
+}
+
+}  // namespace moe

@@ -14,7 +14,9 @@ namespace moe {
 
 // Tiling of the grouped dequant GEMMs (gate_up and down share it).
 constexpr int kBlockRows = 128;   // GEMM rows per work item (gate_up: 64 gate + 64 up rows)
-constexpr int kStageK = 64;       // contraction columns per pipeline stage
+constexpr int kStripRows = 16;    // GEMM rows per compute warp (one m16n8k16 row tile)
+constexpr int kStageCols = 128;   // contraction columns per pipeline stage (the last may have 64)
+constexpr int kBoxCols = 64;      // contraction columns per TMA box of token rows (128 bytes)
 constexpr int kChunkN = 32;       // tokens (pairs) per work item
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;

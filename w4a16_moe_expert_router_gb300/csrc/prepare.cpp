@@ -7,21 +7,23 @@
 // nibble); one fp16 scale and one fp16 zero-point per group of g columns.
 //
 // Prepared stream of one projection (rows R, contraction K, group g), per
-// expert, per block of 128 GEMM rows, per stage of 64 columns:
-//   [(scale, zero) pairs of the block's 128 rows for each group starting in
-//    this stage, 512 bytes per group][4096 bytes of codes]
-// GEMM row r of block b is, for gate_up (R = 2f), gate row 64b+r for r < 64 and
-// up row f+64b+r-64 for r >= 64 (so a block's tensor-memory lanes 0..63 hold
-// gate rows and 64..127 the matching up rows); for down (R = d) it is row
-// 128b+r.  The codes of a stage are ordered [half h][GEMM row r][4 words]:
-// half h covers the stage's columns 32h .. 32h+31, and word w of (h, r) holds the
-// 8 codes of row r at columns c0 = 32h + 8w + {0..7} (relative to the stage),
-// nibble i (bits 4i..4i+3) holding column c0 + {0, 2, 4, 6, 1, 3, 5, 7}[i], the
-// order in which the kernels' dequantiser produces the f16x2 column pairs
-// (c0, c0+1), (c0+2, c0+3), ... it writes to tensor memory.  Each thread of the
-// dequantiser reads its row's two 16-byte halves.
+// expert, per block of 128 GEMM rows, per stage of 128 columns (the last stage
+// has 64 when K is an odd multiple of 64), per warp strip w = 0..7 of 16 GEMM rows:
+//   [(scale, zero) pairs of the strip for the ng groups in this stage, 64 ng bytes]
+//   [codes, 8 bytes per 16 columns per lane]
+// GEMM row r of strip w of block b is, for gate_up (R = 2f), gate row
+// 64b + 8w + r for r < 8 and up row f + 64b + 8w + r - 8 for r >= 8 (so one
+// warp holds a gate row and its up row); for down (R = d) it is row
+// 128b + 16w + r.  The (scale, zero) bytes are ordered [i = 0..7][group j]:
+// 8 bytes holding the (scale, zero) of strip rows i and i + 8 for group j.  The
+// codes are ordered [kk / 4][lane][kk % 4] (one 32-bit word per lane per 16-column
+// step kk of the stage, so a lane reads four steps as one 16-byte vector and a
+// warp's vector is 512 contiguous bytes); word (lane, kk) holds the lane's m16n8k16 A fragment of the 16 columns
+// 16kk.. of the stage: with gq = lane / 4 and tq = lane % 4, nibble i (bits
+// 4i..4i+3) is strip row gq + 8 (i & 1), column 16kk + 2tq + 8 ((i >> 1) & 1) + (i >> 2).
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <vector>
 
@@ -50,18 +52,15 @@ bool proj_of(const moe_w4a16_shape* sh, int32_t which, Proj* p) {
   return true;
 }
 
-// Matrix row of GEMM row r (0..127) of block b.
-inline int64_t gemm_row(const Proj& p, int64_t b, int r) {
-  if (p.gate_up) return r < 64 ? 64 * b + r : p.f + 64 * b + (r - 64);
-  return moe::kBlockRows * b + r;
+constexpr int kStrips = moe::kBlockRows / moe::kStripRows;  // strips per block, one per compute warp
+constexpr int64_t kStageCols = moe::kStageCols;
+
+// Matrix row of row r (0..15) of strip w of block b.
+inline int64_t strip_row(const Proj& p, int64_t b, int w, int r) {
+  if (p.gate_up) return r < 8 ? 64 * b + 8 * w + r : p.f + 64 * b + 8 * w + (r - 8);
+  return moe::kBlockRows * b + 16 * w + r;
 }
 
-inline int groups_in_stage(int64_t s, int64_t g) {
-  return g <= moe::kStageK ? int(moe::kStageK / g) : ((s * moe::kStageK) % g == 0 ? 1 : 0);
-}
-
-// Column offset (within a word's 8 columns) of nibble i of the word.
-constexpr int kNibCol[8] = {0, 2, 4, 6, 1, 3, 5, 7};
 
 double half_value(uint16_t h) {
   const int e = (h >> 10) & 31, m = h & 1023;
@@ -79,35 +78,41 @@ moe_w4a16_status walk(const Proj& p, uint8_t* q, uint16_t* scale, uint16_t* zero
     uint16_t* se = scale + e * p.R * ng;
     uint16_t* ze = zero + e * p.R * ng;
     for (int64_t b = 0; b < p.nblocks; ++b) {
-      int64_t rows[moe::kBlockRows];
-      for (int r = 0; r < moe::kBlockRows; ++r) rows[r] = gemm_row(p, b, r);
-      for (int64_t s = 0; s < p.K / moe::kStageK; ++s) {
-        const int ngs = groups_in_stage(s, p.g);
-        for (int j = 0; j < ngs; ++j) {
-          const int64_t grp = (s * moe::kStageK) / p.g + j;
-          for (int r = 0; r < moe::kBlockRows; ++r) {
-            uint16_t* sp = se + rows[r] * ng + grp;
-            uint16_t* zp = ze + rows[r] * ng + grp;
-            if (kPack) {
-              std::memcpy(out, sp, 2);
-              std::memcpy(out + 2, zp, 2);
-            } else {
-              std::memcpy(sp, out, 2);
-              std::memcpy(zp, out + 2, 2);
+      for (int64_t c0 = 0; c0 < p.K; c0 += kStageCols) {
+        const int64_t width = std::min<int64_t>(kStageCols, p.K - c0);  // 128, or 64 for the last stage
+        const int ngs = int(width / std::min<int64_t>(p.g, width));      // groups in the stage (g divides K)
+        const int steps = int(width / 16);
+        for (int w = 0; w < kStrips; ++w) {
+          int64_t rows[16];
+          for (int r = 0; r < 16; ++r) rows[r] = strip_row(p, b, w, r);
+          for (int i = 0; i < 8; ++i) {
+            for (int j = 0; j < ngs; ++j) {
+              const int64_t grp = c0 / p.g + j;
+              for (int h = 0; h < 2; ++h) {
+                const int r = i + 8 * h;
+                uint16_t* sp = se + rows[r] * ng + grp;
+                uint16_t* zp = ze + rows[r] * ng + grp;
+                if (kPack) {
+                  std::memcpy(out, sp, 2);
+                  std::memcpy(out + 2, zp, 2);
+                } else {
+                  std::memcpy(sp, out, 2);
+                  std::memcpy(zp, out + 2, 2);
+                }
+                out += 4;
+              }
             }
-            out += 4;
           }
-        }
-        for (int hf = 0; hf < 2; ++hf) {
-          for (int r = 0; r < moe::kBlockRows; ++r) {
-            uint8_t* qrow = qe + rows[r] * rowb;
-            for (int w = 0; w < 4; ++w) {
-              const int64_t c0 = s * moe::kStageK + hf * 32 + w * 8;
+          for (int kk = 0; kk < steps; ++kk) {
+            for (int lane = 0; lane < 32; ++lane) {
+              const int gq = lane >> 2, tq = lane & 3;
+              uint8_t* wp = out + (kk / 4) * 512 + lane * 16 + (kk % 4) * 4;
               uint32_t word = 0;
-              if (!kPack) std::memcpy(&word, out, 4);
+              if (!kPack) std::memcpy(&word, wp, 4);
               for (int i = 0; i < 8; ++i) {
-                const int64_t col = c0 + kNibCol[i];
-                uint8_t* byte = qrow + (col >> 1);
+                const int r = gq + 8 * (i & 1);
+                const int64_t col = c0 + 16 * kk + 2 * tq + 8 * ((i >> 1) & 1) + (i >> 2);
+                uint8_t* byte = qe + rows[r] * rowb + (col >> 1);
                 const int sh = (col & 1) ? 4 : 0;
                 if (kPack) {
                   word |= uint32_t((*byte >> sh) & 15u) << (4 * i);
@@ -116,10 +121,10 @@ moe_w4a16_status walk(const Proj& p, uint8_t* q, uint16_t* scale, uint16_t* zero
                   *byte = uint8_t((*byte & ~(15u << sh)) | (code << sh));
                 }
               }
-              if (kPack) std::memcpy(out, &word, 4);
-              out += 4;
+              if (kPack) std::memcpy(wp, &word, 4);
             }
           }
+          out += steps * 128;
         }
       }
     }
