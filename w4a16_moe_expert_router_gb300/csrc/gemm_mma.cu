@@ -27,14 +27,14 @@
 // multiplies w with the fp16 activations into fp32 accumulators (16-column
 // steps in contraction order).
 //
-// Roles of the persistent CTA (two per SM; a stage is 128 contraction columns,
+// Roles of the persistent CTA (three per SM; a stage is 128 contraction columns,
 // the last one 64 when the contraction is an odd multiple of 64):
 //   warp 0      producer: claims items one ahead of use, publishes each in a
 //               small queue in shared memory, and per stage issues one bulk
 //               copy of the stage's weight segment (codes and (scale, zero)
 //               pairs of all eight warps, contiguous in the stream) and two 2-D
 //               TMA loads (64 columns x 32 token rows each, 128-byte swizzle)
-//               of the activations into the same slot of a ring of five;
+//               of the activations into the same slot of a ring of three;
 //   warps 1-8   compute: warp w owns 16 GEMM rows of the block (for gate_up 8
 //               gate rows and the 8 matching up rows, so the gated GELU needs
 //               nothing from another warp).  Per stage each reads its rows'
@@ -61,8 +61,8 @@ namespace {
 
 constexpr int kMmaWarps = kBlockRows / kStripRows;  // compute warps, one 16-row strip each
 constexpr int kThreads = (1 + kMmaWarps) * 32;     // 288
-constexpr int kCtasPerSm = 2;
-constexpr int kSlots = 5;                          // stages in flight per CTA
+constexpr int kCtasPerSm = 3;
+constexpr int kSlots = 3;                          // stages in flight per CTA (three CTAs per SM share 227 KiB)
 constexpr int kQueue = 4;                          // item descriptors in flight per CTA
 constexpr int kBBoxRows = 32;                      // TMA box: 64 columns x 32 token rows
 constexpr int kBoxBytes = kBBoxRows * 128;         // 4 KiB, 128-byte swizzle
@@ -252,12 +252,7 @@ __device__ __forceinline__ bool run_stage(const MmArgs& a, MmHeader& H, volatile
   const uint32_t sl = ring_s + slot * kSlotBytes;
   // this warp's part of the stage's weights: [(scale, zero) x NG][codes]
   const uint32_t wseg = sl + kBBytes + sw * (KK * 128 + kSzBytesW * NG);
-  uint32_t words[KK];
-#pragma unroll
-  for (int q = 0; q < KK / 4; ++q)
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(words[4 * q]), "=r"(words[4 * q + 1]), "=r"(words[4 * q + 2]), "=r"(words[4 * q + 3])
-                 : "r"(wseg + kSzBytesW * NG + q * 512 + lane * 16));
+  const uint32_t caddr = wseg + kSzBytesW * NG + lane * 16;
   uint32_t szw[2 * NG];
   const uint32_t szaddr = wseg + (lane >> 2) * (8 * NG);
   if (NG == 1) {
@@ -270,17 +265,29 @@ __device__ __forceinline__ bool run_stage(const MmArgs& a, MmHeader& H, volatile
                    : "r"(szaddr + 16 * q));
   }
   DqRows k;
+  uint32_t words[4];
 #pragma unroll
   for (int kk = 0; kk < KK; ++kk) {
+    if (kk % 4 == 0)
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(words[0]), "=r"(words[1]), "=r"(words[2]), "=r"(words[3])
+                   : "r"(caddr + (kk / 4) * 512));
     if (kk % kStepsPerGroup == 0) k = dq_rows(szw[2 * (kk / kStepsPerGroup)], szw[2 * (kk / kStepsPerGroup) + 1]);
     uint32_t af[4];
-    dequant_frag(words[kk], k, af);
-    uint32_t b[4][2];
+    dequant_frag(words[kk % 4], k, af);
     const uint32_t baddr = sl + (kk / 4) * kBoxBytes + loff[kk % 4];
-    ldmatrix_x4(baddr, b[0][0], b[0][1], b[1][0], b[1][1]);
-    if (NT > 2) ldmatrix_x4(baddr + 16 * 128, b[2][0], b[2][1], b[3][0], b[3][1]);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mma_f16_16816(acc[nt], af, b[nt][0], b[nt][1]);
+    {
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4(baddr, b0, b1, b2, b3);
+      mma_f16_16816(acc[0], af, b0, b1);
+      if (NT > 1) mma_f16_16816(acc[NT > 1 ? 1 : 0], af, b2, b3);
+    }
+    if (NT > 2) {
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4(baddr + 16 * 128, b0, b1, b2, b3);
+      mma_f16_16816(acc[NT > 2 ? 2 : 0], af, b0, b1);
+      if (NT > 3) mma_f16_16816(acc[NT > 3 ? 3 : 0], af, b2, b3);
+    }
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_addr(&H.slot_empty[slot]));  // shared-memory reads of the stage done
