@@ -19,7 +19,7 @@
 // registers of an m16n8k16 A fragment and hands them to the MMA itself; no
 // weight tile is written to shared or tensor memory and no other warp has to be
 // told that it is ready.  The tokens (the B operand) are shared by the CTA's
-// eight compute warps through a TMA-filled shared-memory ring.
+// four compute warps through a TMA-filled shared-memory ring.
 //
 // Arithmetic: the zero-point is split into its nearest integer zr and the rest
 // zf = z - zr, and each weight is formed as w = fp16((q - zr) * s - fp16(zf * s)):
@@ -32,18 +32,22 @@
 //   warp 0      producer: claims items one ahead of use, publishes each in a
 //               small queue in shared memory, and per stage issues one bulk
 //               copy of the stage's weight segment (codes and (scale, zero)
-//               pairs of all eight warps, contiguous in the stream) and two 2-D
-//               TMA loads (64 columns x 32 token rows each, 128-byte swizzle)
-//               of the activations into the same slot of a ring of three;
-//   warps 1-8   compute: warp w owns 16 GEMM rows of the block (for gate_up 8
-//               gate rows and the 8 matching up rows, so the gated GELU needs
-//               nothing from another warp).  Per stage each reads its rows'
-//               codes (16-byte vectors, 512 contiguous bytes per warp) and
-//               (scale, zero) pairs from the slot, dequantises them into A
-//               fragments, reads the token fragments with ldmatrix and issues
-//               the MMAs; an item's accumulators stay in registers.  The
-//               kernel is specialised per item on the token tiles (1-4 tiles
-//               of 8) and the group size, so a stage has no data-dependent
+//               pairs of all eight 16-row strips, contiguous in the stream) and
+//               two 2-D TMA loads (64 columns x 32 token rows each, 128-byte
+//               swizzle) of the activations into the same slot of a ring of
+//               three;
+//   warps 1-4   compute: warp w owns strips 2w and 2w+1, 32 GEMM rows of the
+//               block (a gate_up strip holds 8 gate rows and the 8 matching up
+//               rows, so the gated GELU needs nothing from another warp).  Per
+//               stage each reads its strips' codes (16-byte vectors, 512
+//               contiguous bytes per strip and load) and (scale, zero) pairs
+//               from the slot, dequantises them into A fragments, reads each
+//               token fragment once with ldmatrix for both strips and issues
+//               the MMAs; an item's accumulators stay in registers.  Two
+//               strips per warp share the token fragments, the waits and the
+//               address work, and give each warp twice the independent work.
+//               The kernel is specialised per item on the token tiles (1-4
+//               tiles of 8) and the group size, so a stage has no data-dependent
 //               branches.
 // Every wait is bounded: on expiry the CTA records MOE_W4A16_ERR_TIMEOUT in the
 // workspace and all roles leave their loops; the producer drains its copies.
@@ -59,8 +63,9 @@
 namespace moe {
 namespace {
 
-constexpr int kMmaWarps = kBlockRows / kStripRows;  // compute warps, one 16-row strip each
-constexpr int kThreads = (1 + kMmaWarps) * 32;     // 288
+constexpr int kStrips = kBlockRows / kStripRows;   // 16-row strips per block
+constexpr int kMmaWarps = kStrips / 2;             // compute warps, two strips each
+constexpr int kThreads = (1 + kMmaWarps) * 32;     // 160
 constexpr int kCtasPerSm = 3;
 constexpr int kSlots = 3;                          // stages in flight per CTA (three CTAs per SM share 227 KiB)
 constexpr int kQueue = 4;                          // item descriptors in flight per CTA
@@ -68,7 +73,7 @@ constexpr int kBBoxRows = 32;                      // TMA box: 64 columns x 32 t
 constexpr int kBoxBytes = kBBoxRows * 128;         // 4 KiB, 128-byte swizzle
 constexpr int kBBytes = 2 * kBoxBytes;             // a stage's token tile: two boxes
 constexpr int kSzBytesW = 64;                      // one warp's (scale, zero) pairs of one group
-constexpr int kWMaxBytes = kMmaWarps * (1024 + 4 * kSzBytesW);  // a stage's weights, at most 10 KiB
+constexpr int kWMaxBytes = kStrips * (1024 + 4 * kSzBytesW);  // a stage's weights, at most 10 KiB
 constexpr int kSlotBytes = 18432;                  // [tokens 8 KiB][weights <= 10 KiB], a multiple of 1024
 static_assert(kBBytes + kWMaxBytes <= kSlotBytes && kSlotBytes % 1024 == 0, "slot layout");
 constexpr int kHeaderBytes = 4096;
@@ -114,7 +119,7 @@ static_assert(sizeof(MmHeader) <= kHeaderBytes, "header fits");
 // Weight bytes of one stage of kk16 16-column steps (all eight warps) with groups of g.
 __device__ __forceinline__ uint32_t stage_weight_bytes(int kk16, int g) {
   const int ng = (16 * kk16) / min(g, 16 * kk16);
-  return static_cast<uint32_t>(kMmaWarps * (kk16 * 128 + kSzBytesW * ng));
+  return static_cast<uint32_t>(kStrips * (kk16 * 128 + kSzBytesW * ng));
 }
 
 __device__ __forceinline__ int expert_of(int item, const int* prefix, int E) {
@@ -241,52 +246,69 @@ __device__ __forceinline__ bool read_item(const MmHeader& H, int i, const MmArgs
   return true;
 }
 
-// One stage of one compute warp: KK 16-column steps, NT tiles of 8 tokens, groups of G.
+// One stage of one compute warp: KK 16-column steps, NT tiles of 8 tokens, groups of G,
+// for the warp's two strips 2 sw and 2 sw + 1 (one token fragment serves both).
 template <int NT, int G, int KK>
-__device__ __forceinline__ bool run_stage(const MmArgs& a, MmHeader& H, volatile int* abort, float (&acc)[NT][4],
-                                          int& slot, uint32_t& phase, uint32_t ring_s, const uint32_t (&loff)[4],
-                                          int sw, int lane) {
+__device__ __forceinline__ bool run_stage(const MmArgs& a, MmHeader& H, volatile int* abort,
+                                          float (&acc)[2][NT][4], int& slot, uint32_t& phase, uint32_t ring_s,
+                                          const uint32_t (&loff)[4], int sw, int lane) {
   constexpr int NG = (16 * KK) / (G < 16 * KK ? G : 16 * KK);  // groups in the stage
   constexpr int kStepsPerGroup = KK / NG;
+  constexpr int kStripBytes = KK * 128 + kSzBytesW * NG;
   if (!warp_wait(smem_addr(&H.slot_full[slot]), phase, a, abort)) return false;
   const uint32_t sl = ring_s + slot * kSlotBytes;
-  // this warp's part of the stage's weights: [(scale, zero) x NG][codes]
-  const uint32_t wseg = sl + kBBytes + sw * (KK * 128 + kSzBytesW * NG);
+  // the warp's strips of the stage's weights: [(scale, zero) x NG][codes], one after the other
+  const uint32_t wseg = sl + kBBytes + 2 * sw * kStripBytes;
   const uint32_t caddr = wseg + kSzBytesW * NG + lane * 16;
-  uint32_t szw[2 * NG];
-  const uint32_t szaddr = wseg + (lane >> 2) * (8 * NG);
-  if (NG == 1) {
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(szw[0]), "=r"(szw[1]) : "r"(szaddr));
-  } else {
+  uint32_t szw[2][2 * NG];
 #pragma unroll
-    for (int q = 0; q < NG / 2; ++q)
-      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(szw[4 * q]), "=r"(szw[4 * q + 1]), "=r"(szw[4 * q + 2]), "=r"(szw[4 * q + 3])
-                   : "r"(szaddr + 16 * q));
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t szaddr = wseg + h * kStripBytes + (lane >> 2) * (8 * NG);
+    if (NG == 1) {
+      asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(szw[h][0]), "=r"(szw[h][1]) : "r"(szaddr));
+    } else {
+#pragma unroll
+      for (int q = 0; q < NG / 2; ++q)
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(szw[h][4 * q]), "=r"(szw[h][4 * q + 1]), "=r"(szw[h][4 * q + 2]), "=r"(szw[h][4 * q + 3])
+                     : "r"(szaddr + 16 * q));
+    }
   }
-  DqRows k;
-  uint32_t words[4];
+  DqRows k[2];
+  uint32_t words[2][4];
 #pragma unroll
   for (int kk = 0; kk < KK; ++kk) {
     if (kk % 4 == 0)
-      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(words[0]), "=r"(words[1]), "=r"(words[2]), "=r"(words[3])
-                   : "r"(caddr + (kk / 4) * 512));
-    if (kk % kStepsPerGroup == 0) k = dq_rows(szw[2 * (kk / kStepsPerGroup)], szw[2 * (kk / kStepsPerGroup) + 1]);
-    uint32_t af[4];
-    dequant_frag(words[kk % 4], k, af);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(words[h][0]), "=r"(words[h][1]), "=r"(words[h][2]), "=r"(words[h][3])
+                     : "r"(caddr + h * kStripBytes + (kk / 4) * 512));
+    if (kk % kStepsPerGroup == 0)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        k[h] = dq_rows(szw[h][2 * (kk / kStepsPerGroup)], szw[h][2 * (kk / kStepsPerGroup) + 1]);
+    uint32_t af[2][4];
+    dequant_frag(words[0][kk % 4], k[0], af[0]);
+    dequant_frag(words[1][kk % 4], k[1], af[1]);
     const uint32_t baddr = sl + (kk / 4) * kBoxBytes + loff[kk % 4];
     {
       uint32_t b0, b1, b2, b3;
       ldmatrix_x4(baddr, b0, b1, b2, b3);
-      mma_f16_16816(acc[0], af, b0, b1);
-      if (NT > 1) mma_f16_16816(acc[NT > 1 ? 1 : 0], af, b2, b3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        mma_f16_16816(acc[h][0], af[h], b0, b1);
+        if (NT > 1) mma_f16_16816(acc[h][NT > 1 ? 1 : 0], af[h], b2, b3);
+      }
     }
     if (NT > 2) {
       uint32_t b0, b1, b2, b3;
       ldmatrix_x4(baddr + 16 * 128, b0, b1, b2, b3);
-      mma_f16_16816(acc[NT > 2 ? 2 : 0], af, b0, b1);
-      if (NT > 3) mma_f16_16816(acc[NT > 3 ? 3 : 0], af, b2, b3);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        mma_f16_16816(acc[h][NT > 2 ? 2 : 0], af[h], b0, b1);
+        if (NT > 3) mma_f16_16816(acc[h][NT > 3 ? 3 : 0], af[h], b2, b3);
+      }
     }
   }
   __syncwarp();
@@ -305,11 +327,13 @@ __device__ __forceinline__ bool run_item(const MmArgs& a, MmHeader& H, volatile 
                                          int& slot, uint32_t& phase, uint32_t ring_s, const uint32_t (&loff)[4],
                                          int sw, int lane) {
   const int gq = lane >> 2, tq = lane & 3;
-  float acc[NT][4];
+  float acc[2][NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int h = 0; h < 2; ++h)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[nt][j] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[h][nt][j] = 0.f;
   const int K = a.p[v.pj].K;
   for (int c0 = 0; c0 + kStageCols <= K; c0 += kStageCols)
     if (!run_stage<NT, G, 8>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
@@ -317,17 +341,20 @@ __device__ __forceinline__ bool run_item(const MmArgs& a, MmHeader& H, volatile 
     if (!run_stage<NT, (G < 64 ? G : 64), 4>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
   // ------------------------------------------------------------------ epilogue
   if (v.pj == 0) {
-    // rows gq: gate j, gq + 8: up j, with j = 64 * blk + 8 * sw + gq
-    const int j = 64 * v.blk + 8 * sw + gq;
+    // strip s: rows gq gate j, gq + 8 up j, with j = 64 * blk + 8 * s + gq
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int n = 8 * nt + 2 * tq;
-      if (n < v.n_cnt)
-        a.h[static_cast<size_t>(v.pos0 + n) * a.f + j] =
-            __half_as_ushort(__float2half_rn(gelu(acc[nt][0], a.act) * acc[nt][2]));
-      if (n + 1 < v.n_cnt)
-        a.h[static_cast<size_t>(v.pos0 + n + 1) * a.f + j] =
-            __half_as_ushort(__float2half_rn(gelu(acc[nt][1], a.act) * acc[nt][3]));
+    for (int h = 0; h < 2; ++h) {
+      const int j = 64 * v.blk + 8 * (2 * sw + h) + gq;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int n = 8 * nt + 2 * tq;
+        if (n < v.n_cnt)
+          a.h[static_cast<size_t>(v.pos0 + n) * a.f + j] =
+              __half_as_ushort(__float2half_rn(gelu(acc[h][nt][0], a.act) * acc[h][nt][2]));
+        if (n + 1 < v.n_cnt)
+          a.h[static_cast<size_t>(v.pos0 + n + 1) * a.f + j] =
+              __half_as_ushort(__float2half_rn(gelu(acc[h][nt][1], a.act) * acc[h][nt][3]));
+      }
     }
     if (a.last == 1) {
       // report the h rows to the expert's counter: __syncwarp orders the lanes' stores before
@@ -336,19 +363,24 @@ __device__ __forceinline__ bool run_item(const MmArgs& a, MmHeader& H, volatile 
       if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a.gu_done + v.e) : "memory");
     }
   } else {
-    const int i_row = kBlockRows * v.blk + 16 * sw + gq;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int n = 8 * nt + 2 * tq;
-      if (n < v.n_cnt) {
-        float* yr = a.y_out + static_cast<size_t>(a.pair_list[v.pos0 + n]) * a.d + i_row;
-        yr[0] = acc[nt][0];
-        yr[8] = acc[nt][2];
-      }
-      if (n + 1 < v.n_cnt) {
-        float* yr = a.y_out + static_cast<size_t>(a.pair_list[v.pos0 + n + 1]) * a.d + i_row;
-        yr[0] = acc[nt][1];
-        yr[8] = acc[nt][3];
+      const int p0 = n < v.n_cnt ? a.pair_list[v.pos0 + n] : 0;
+      const int p1 = n + 1 < v.n_cnt ? a.pair_list[v.pos0 + n + 1] : 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i_row = kBlockRows * v.blk + 16 * (2 * sw + h) + gq;
+        if (n < v.n_cnt) {
+          float* yr = a.y_out + static_cast<size_t>(p0) * a.d + i_row;
+          yr[0] = acc[h][nt][0];
+          yr[8] = acc[h][nt][2];
+        }
+        if (n + 1 < v.n_cnt) {
+          float* yr = a.y_out + static_cast<size_t>(p1) * a.d + i_row;
+          yr[0] = acc[h][nt][1];
+          yr[8] = acc[h][nt][3];
+        }
       }
     }
   }
@@ -507,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ compute warps
-    const int sw = warp - 1;  // the warp's 16 rows of the block
+    const int sw = warp - 1;  // the warp's strips 2 sw and 2 sw + 1 of the block
     // ldmatrix: lanes 0-7 / 8-15 / 16-23 / 24-31 address token rows 0-7 / 0-7 / 8-15 / 8-15 at the
     // step's first / second / first / second 8 columns; the token tile is 128-byte swizzled (the
     // 16-byte chunk c of token row n sits at chunk c ^ (n & 7))
