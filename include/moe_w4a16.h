@@ -251,6 +251,19 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_forward_noalloc(const moe_w4a16_shape* 
                                                          float norm_eps, uint16_t* out, void* stream);
 
 /* Static description of a status code (never NULL). */
+/* Self-test of the device-side failure path.  Every wait in the expert launch
+ * (on its mbarrier rings and on the counters other CTAs raise) is bounded: on
+ * expiry the kernel records MOE_W4A16_ERR_TIMEOUT in the workspace's error
+ * word, every role of the CTA leaves its loop, in-flight copies are drained and
+ * the kernel returns, so the context stays usable.  This call launches one warp
+ * that runs the same wait helpers, with bound limit_ns, on an mbarrier phase
+ * that nothing completes and on a workspace counter that nothing raises; both
+ * give up and moe_w4a16_read_error then reports MOE_W4A16_ERR_TIMEOUT (clear it
+ * with moe_w4a16_workspace_init).  The workspace must have been initialised.
+ *   limit_ns  1 .. 2e9 (ERR_VALUE otherwise); the call takes about 2 limit_ns on the device. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_selftest_wait_timeout(void* workspace, size_t workspace_bytes,
+                                                               uint64_t limit_ns, void* stream);
+
 MOE_W4A16_API const char* moe_w4a16_status_string(moe_w4a16_status status);
 
 #ifdef __cplusplus

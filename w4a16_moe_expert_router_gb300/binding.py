@@ -25,7 +25,8 @@ GATE_UP, DOWN = 0, 1
 EXPORTED = ("moe_w4a16_workspace_bytes", "moe_w4a16_workspace_init", "moe_w4a16_route", "moe_w4a16_forward",
             "moe_w4a16_experts",
             "moe_w4a16_gate_up", "moe_w4a16_down", "moe_w4a16_combine", "moe_w4a16_read_error", "moe_w4a16_pack", "moe_w4a16_unpack", "moe_w4a16_prepared_bytes",
-            "moe_w4a16_prepare", "moe_w4a16_unprepare", "moe_w4a16_status_string", "moe_w4a16_forward_noalloc")
+            "moe_w4a16_prepare", "moe_w4a16_unprepare", "moe_w4a16_status_string", "moe_w4a16_forward_noalloc",
+            "moe_w4a16_selftest_wait_timeout")
 
 NOALLOC_SCRATCH_BYTES = 40 << 20  # MOE_W4A16_NOALLOC_SCRATCH_BYTES
 
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
             L.moe_w4a16_forward_noalloc.argtypes = [P(Shape), vp, P(Routing), P(Weights), vp, ctypes.c_float, vp,
                                                     vp]
             L.moe_w4a16_forward_noalloc.restype = st
+            L.moe_w4a16_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint64, vp]
+            L.moe_w4a16_selftest_wait_timeout.restype = st
             L.moe_w4a16_read_error.argtypes = [vp, sz, vp, P(ctypes.c_int)]
             L.moe_w4a16_read_error.restype = st
             L.moe_w4a16_pack.argtypes = [vp, i64, i64, vp]
@@ -225,6 +228,11 @@ def moe_w4a16_read_error(workspace, stream=None) -> int:
     _check(lib().moe_w4a16_read_error(_dptr(workspace), _nbytes(workspace), _stream(stream), ctypes.byref(code)),
            "moe_w4a16_read_error")
     return code.value
+
+
+def moe_w4a16_selftest_wait_timeout(workspace, limit_ns: int, stream=None) -> None:
+    _check(lib().moe_w4a16_selftest_wait_timeout(_dptr(workspace), _nbytes(workspace), limit_ns, _stream(stream)),
+           "moe_w4a16_selftest_wait_timeout")
 
 
 def moe_w4a16_pack(codes: np.ndarray) -> np.ndarray:

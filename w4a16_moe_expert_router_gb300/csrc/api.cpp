@@ -89,6 +89,19 @@ moe_w4a16_status moe_w4a16_workspace_init(void* workspace, size_t workspace_byte
   return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(moe::WsHeader), static_cast<cudaStream_t>(stream)));
 }
 
+moe_w4a16_status moe_w4a16_selftest_wait_timeout(void* workspace, size_t workspace_bytes, uint64_t limit_ns,
+                                                void* stream) {
+  if (!workspace) return MOE_W4A16_ERR_NULL;
+  if (!aligned16(workspace)) return MOE_W4A16_ERR_ALIGN;
+  if (workspace_bytes < sizeof(moe::WsHeader)) return MOE_W4A16_ERR_WORKSPACE;
+  if (limit_ns == 0 || limit_ns > 2000000000ull) return MOE_W4A16_ERR_VALUE;
+  moe_w4a16_status st;
+  const DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != MOE_W4A16_OK) return st;
+  auto* hdr = static_cast<moe::WsHeader*>(workspace);
+  return cuda_status(moe::launch_wait_selftest(&hdr->error, &hdr->never_set, limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
 moe_w4a16_status moe_w4a16_route(const moe_w4a16_shape* shape, const float* logits, const moe_w4a16_routing* out,
                                  void* workspace, size_t workspace_bytes, void* stream) {
   Dims s;

@@ -211,7 +211,8 @@ __device__ __forceinline__ float gelu(float a, int act) {
 // Warp-uniform bounded wait: every lane polls the barrier (so each acquires the
 // phase), the warp leaves together once all lanes have seen it complete, and the
 // decision to give up is lane 0's, broadcast.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const MmArgs& a, volatile int* abort) {
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t* err, volatile int* abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
@@ -219,13 +220,34 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const M
     int give_up = 0;
     if ((threadIdx.x & 31) == 0) {
       give_up = *abort != 0;
-      if (!give_up && global_timer_ns() - t0 > kWaitLimitNs) {
-        atomicExch(a.err, kStatusTimeout);
+      if (!give_up && global_timer_ns() - t0 > limit_ns) {
+        atomicExch(err, kStatusTimeout);
         *abort = 1;
         give_up = 1;
       }
     }
     if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
+  }
+}
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const MmArgs& a, volatile int* abort) {
+  return warp_wait(bar, parity, a.err, abort);
+}
+
+// Bounded wait by one thread until a device-scope counter written by other CTAs
+// reaches need (acquire: their writes released before the count are visible).
+__device__ __forceinline__ bool wait_count(const int32_t* ctr, int need, int32_t* err, volatile int* abort,
+                                           uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= need) return true;
+    if (*abort || global_timer_ns() - t0 > limit_ns) {
+      atomicExch(err, kStatusTimeout);
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(256);
   }
 }
 
@@ -489,19 +511,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // expert has written them
         if (lane == 0) {
           const int need = kMmaWarps * a.p[0].nblocks * ((H.offs[e + 1] - H.offs[e] + kChunkN - 1) / kChunkN);
-          const uint64_t t0 = global_timer_ns();
-          for (;;) {
-            int v;
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.gu_done + e) : "memory");
-            if (v >= need) break;
-            if (*abort || global_timer_ns() - t0 > kDepWaitNs) {
-              atomicExch(a.err, kStatusTimeout);
-              *abort = 1;
-              ok = false;
-              break;
-            }
-            __nanosleep(256);
-          }
+          ok = wait_count(a.gu_done + e, need, a.err, abort, kDepWaitNs);
           // the TMA loads below read those rows through the async proxy
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
@@ -573,6 +583,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
 }
 
+// Self-test of the bounded waits above: one warp waits, with the given bound, on
+// an mbarrier phase that nothing completes and then on a counter that nothing
+// raises (flag, left at 0); each wait gives up, records MOE_W4A16_ERR_TIMEOUT in
+// *err and the kernel returns.  Nothing is in flight when it returns.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(int32_t* err, const int32_t* flag, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);  // one arrival that never comes
+    abort = 0;
+    fence_barrier_init();
+  }
+  __syncwarp();
+  volatile int* ab = &abort;
+  warp_wait(smem_addr(&bar), 0, err, ab, limit_ns);
+  __syncwarp();
+  if (threadIdx.x == 0) {
+    *ab = 0;  // the counter wait is timed on its own
+    wait_count(flag, 1, err, ab, limit_ns);
+  }
+}
+
 // Token rows of every (token, expert) pair, copied in expert-sorted order:
 // xs[pos] = x[pair_list[pos] / k].  One warp per row, 16-byte accesses.  Also
 // clears the per-expert gate_up counters that the GEMM launch after it counts up.
@@ -638,6 +670,11 @@ cudaError_t init_gemm_kernels(int* blocks_per_sm) {
   if (err != cudaSuccess) return err;
   *blocks_per_sm = kCtasPerSm;
   return cudaSuccess;
+}
+
+cudaError_t launch_wait_selftest(int32_t* err, const int32_t* flag, uint64_t limit_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(err, flag, limit_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, const int32_t* expert_offsets,

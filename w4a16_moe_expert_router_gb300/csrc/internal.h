@@ -27,7 +27,8 @@ struct WsHeader {
   int32_t error;          // sticky moe_w4a16_status of device-side failures
   int32_t next_item[2];   // work counters of GEMM launches with gate_up items (0) and of down-only launches (1)
   int32_t done_ctas[2];   // CTAs of such a launch that have finished (the last resets both)
-  int32_t pad[59];
+  int32_t never_set;      // stays 0: the counter the wait self-test waits on
+  int32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -104,5 +105,10 @@ cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, cons
 
 cudaError_t launch_combine(const Dims& s, const float* topk_w, const float* y, const float* gamma, float eps,
                            uint16_t* out, cudaStream_t st);
+
+// Self-test of the expert launch's bounded waits: waits that cannot complete (an
+// mbarrier phase, then the counter *flag, which must stay 0) give up after limit_ns
+// each and record MOE_W4A16_ERR_TIMEOUT in *err.
+cudaError_t launch_wait_selftest(int32_t* err, const int32_t* flag, uint64_t limit_ns, cudaStream_t st);
 
 }  // namespace moe
