@@ -10,9 +10,11 @@
 // Two launches.  The first ranks the experts of every token (one warp per
 // token, eight tokens per CTA, so even a 256-token canvas spreads over 32 SMs)
 // and, per CTA, counts its pairs per expert and ranks each pair among the
-// CTA's earlier pairs of the same expert.  The second, one CTA launched with
-// programmatic dependent launch, turns the per-CTA counts into positions
-// (exclusive scans over CTAs, then over experts) and places every pair.
+// CTA's earlier pairs of the same expert.  The second, launched with
+// programmatic dependent launch, has one CTA per CTA of the first: each reads
+// the whole table of per-CTA counts (one parallel round of loads), forms the
+// expert totals, their exclusive scan (the expert offsets) and its own CTA's
+// prefix per expert, and places that CTA's pairs.
 #include <cfloat>
 #include <climits>
 
@@ -23,8 +25,7 @@ namespace moe {
 namespace {
 
 constexpr int kTopkWarps = 8;        // tokens per CTA of the top-k launch
-constexpr int kGroupThreads = 1024;  // the grouping CTA
-constexpr int kScanSplit = kGroupThreads / kMaxExperts;  // threads per expert in the scan over CTAs
+constexpr int kGroupThreads = 256;   // a grouping CTA: one thread per expert (E <= 256)
 
 // Router order as one unsigned key: a larger logit gives a larger key, -0 and
 // +0 give the same key (they compare equal as fp32 values); NaN ranks below
@@ -139,87 +140,55 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __re
   for (int e = tid; e < E; e += kTopkWarps * 32) cta_hist[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
 }
 
-// One CTA: per expert, the exclusive scan of the per-CTA counts over the CTAs
-// (written back in place), the expert offsets (exclusive scan over experts), and
-// every pair placed at offset + earlier CTAs' count + its rank in its CTA.
+// Grouping CTA c (one per top-k CTA): thread e sums the counts of expert e over
+// all top-k CTAs (its total) and over CTAs before c (its prefix for CTA c); the
+// exclusive scan of the totals gives the expert offsets; then CTA c places its
+// own pairs at offset + prefix + rank in the CTA.  CTA 0 also writes the offsets.
 __global__ void __launch_bounds__(kGroupThreads) group_kernel(const int32_t* __restrict__ topk_idx, int P, int E,
-                                                              int k, int nctas, int32_t* __restrict__ cta_hist,
+                                                              int k, int nctas, const int32_t* __restrict__ cta_hist,
                                                               const int32_t* __restrict__ local_rank,
                                                               int32_t* __restrict__ expert_offsets,
                                                               int32_t* __restrict__ pair_list) {
-  __shared__ int base[kMaxExperts];
-  __shared__ int tot[kMaxExperts];
+  __shared__ int pos_base[kMaxExperts];  // offset of expert e + the count of e in CTAs before this one
+  __shared__ int warp_tot[kGroupThreads / 32];
   grid_dependents_launch();
   grid_dependency_wait();  // the top-k launch's outputs
-  __shared__ int part[kMaxExperts][kScanSplit];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // per expert, kScanSplit threads each own a contiguous range of CTAs: their sums, an
-  // exclusive scan of those sums, then each range's prefixes written back in place
-  const int e_s = tid / kScanSplit, sub = tid % kScanSplit;
-  const int per = (nctas + kScanSplit - 1) / kScanSplit;
-  const int c_lo = sub * per, c_hi = min(nctas, c_lo + per);
-  if (e_s < E) {
-    int sum = 0;
-#pragma unroll 8
-    for (int c = c_lo; c < c_hi; ++c) sum += cta_hist[static_cast<size_t>(c) * E + e_s];
-    part[e_s][sub] = sum;
-  }
-  __syncthreads();
-  if (e_s < E) {
-    int run = 0;
-    for (int j = 0; j < sub; ++j) run += part[e_s][j];
-    if (sub == kScanSplit - 1) tot[e_s] = run + part[e_s][sub];
-#pragma unroll 8
-    for (int c = c_lo; c < c_hi; ++c) {
-      const int h = cta_hist[static_cast<size_t>(c) * E + e_s];
-      cta_hist[static_cast<size_t>(c) * E + e_s] = run;
-      run += h;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, c = blockIdx.x;
+  const int e = tid;
+  int tot = 0, pre = 0;
+  if (e < E) {
+#pragma unroll 16
+    for (int cc = 0; cc < nctas; ++cc) {
+      const int h = cta_hist[static_cast<size_t>(cc) * E + e];
+      tot += h;
+      pre += cc < c ? h : 0;
     }
   }
-  __syncthreads();
-  if (warp == 0) {  // exclusive scan of the expert totals: lane owns 8 consecutive experts
-    int local[8], sum = 0;
+  // exclusive scan of the totals over the experts (thread e holds expert e)
+  int incl = tot;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = lane * 8 + j;
-      local[j] = sum;
-      sum += e < E ? tot[e] : 0;
-    }
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
-    }
-    const int excl = incl - sum;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = lane * 8 + j;
-      if (e < E) {
-        base[e] = excl + local[j];
-        expert_offsets[e] = excl + local[j];
-      }
-    }
-    if (lane == 31) expert_offsets[E] = incl;
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
   }
+  if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
-  const int pairs_per_cta = kTopkWarps * k;
-  constexpr int kU = 4;  // pairs per thread per round, their loads issued together
-  for (int p0 = tid; p0 < P; p0 += kU * kGroupThreads) {
-    int e[kU], lr[kU], h[kU];
+  int before = 0;
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int p = p0 + u * kGroupThreads;
-      e[u] = p < P ? topk_idx[p] : -1;
-      lr[u] = p < P ? local_rank[p] : 0;
-      if (static_cast<unsigned>(e[u]) >= static_cast<unsigned>(E)) e[u] = -1;
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u)
-      h[u] = e[u] >= 0 ? cta_hist[static_cast<size_t>((p0 + u * kGroupThreads) / pairs_per_cta) * E + e[u]] : 0;
-#pragma unroll
-    for (int u = 0; u < kU; ++u)
-      if (e[u] >= 0) pair_list[base[e[u]] + h[u] + lr[u]] = p0 + u * kGroupThreads;
+  for (int w = 0; w < kGroupThreads / 32; ++w) before += w < warp ? warp_tot[w] : 0;
+  const int offset = before + incl - tot;
+  if (e < E) {
+    pos_base[e] = offset + pre;
+    if (c == 0) expert_offsets[e] = offset;
+  }
+  if (c == 0 && e == E - 1) expert_offsets[E] = offset + tot;
+  __syncthreads();
+  // this CTA's pairs: p = c * (tokens per top-k CTA * k) + i
+  const int pairs_per_cta = kTopkWarps * k;  // <= 64
+  const int p = c * pairs_per_cta + tid;
+  if (tid < pairs_per_cta && p < P) {
+    const int ep = topk_idx[p];
+    if (static_cast<unsigned>(ep) < static_cast<unsigned>(E)) pair_list[pos_base[ep] + local_rank[p]] = p;
   }
 }
 
@@ -234,8 +203,8 @@ cudaError_t launch_route(const Dims& s, const float* logits, int32_t* topk_idx, 
   cudaError_t err = launch_pdl(topk_kernel, dim3(nctas), dim3(kTopkWarps * 32), 0, st, logits, s.T, s.E, s.k,
                                topk_idx, topk_w, cta_hist, local_rank);
   if (err != cudaSuccess) return err;
-  return launch_pdl(group_kernel, dim3(1), dim3(kGroupThreads), 0, st, static_cast<const int32_t*>(topk_idx),
-                    static_cast<int>(s.pairs()), s.E, s.k, nctas, cta_hist,
+  return launch_pdl(group_kernel, dim3(nctas), dim3(kGroupThreads), 0, st, static_cast<const int32_t*>(topk_idx),
+                    static_cast<int>(s.pairs()), s.E, s.k, nctas, static_cast<const int32_t*>(cta_hist),
                     static_cast<const int32_t*>(local_rank), expert_offsets, pair_list);
 }
 
