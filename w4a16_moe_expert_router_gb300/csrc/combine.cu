@@ -4,7 +4,9 @@
 // Model card "srswti/axe-diffusion-ksl-xe", "the kernels we built": the weighted
 // combine uses a fixed-order reduction instead of index_add_, because a 1-ulp
 // difference from atomics can flip a block-diffusion acceptance threshold; and
-// RMSNorm collapses into a single launch.  Here one CTA owns one token row:
+// RMSNorm collapses into a single launch.  With RMSNorm one CTA owns one token
+// row (the norm needs the whole row); without it four 128-thread CTAs share a
+// row, a quarter each (more CTAs to spread the reads over the SMs):
 //   u[i]   = w[t][0] y[t*k][i] + ... + w[t][k-1] y[t*k+k-1][i]   (fp32, rank order, fused multiply-adds)
 //   out[i] = fp16(u[i])                                         without gamma
 //   out[i] = fp16(gamma[i] * u[i] / sqrt(mean(u^2) + eps))       with gamma
@@ -95,13 +97,47 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restri
   }
 }
 
+// Without RMSNorm: one 128-thread CTA per quarter of a token row (d / 4 columns,
+// one float4 per thread and row), the same arithmetic in the same order.
+__global__ void __launch_bounds__(128) combine_quarter_kernel(const float* __restrict__ topk_w,
+                                                             const float* __restrict__ y, int d, int k,
+                                                             uint16_t* __restrict__ out) {
+  grid_dependents_launch();
+  grid_dependency_wait();
+  const int t = blockIdx.x >> 2, q = blockIdx.x & 3;
+  const int n4 = d >> 2;
+  const float4* y4 = reinterpret_cast<const float4*>(y) + static_cast<size_t>(t) * k * n4;
+  uint2* o2 = reinterpret_cast<uint2*>(out + static_cast<size_t>(t) * d);
+  for (int i4 = q * (n4 >> 2) + threadIdx.x; i4 < (q + 1) * (n4 >> 2); i4 += 128) {
+    float wr[kMaxTopK];
+    float4 v[kMaxTopK];
+#pragma unroll
+    for (int r = 0; r < kMaxTopK; ++r)
+      if (r < k) {
+        wr[r] = topk_w[static_cast<size_t>(t) * k + r];
+        v[r] = y4[static_cast<size_t>(r) * n4 + i4];
+      }
+    float4 acc = make_float4(wr[0] * v[0].x, wr[0] * v[0].y, wr[0] * v[0].z, wr[0] * v[0].w);
+#pragma unroll
+    for (int r = 1; r < kMaxTopK; ++r)
+      if (r < k) {
+        acc.x = fmaf(wr[r], v[r].x, acc.x);
+        acc.y = fmaf(wr[r], v[r].y, acc.y);
+        acc.z = fmaf(wr[r], v[r].z, acc.z);
+        acc.w = fmaf(wr[r], v[r].w, acc.w);
+      }
+    const __half2 lo = __floats2half2_rn(acc.x, acc.y);
+    const __half2 hi = __floats2half2_rn(acc.z, acc.w);
+    o2[i4] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const Dims& s, const float* topk_w, const float* y, const float* gamma, float eps,
                            uint16_t* out, cudaStream_t st) {
   if (gamma) return launch_pdl(combine_kernel<true>, dim3(s.T), dim3(kThreads), 0, st, topk_w, y, s.d, s.k, gamma, eps, out);
-  return launch_pdl(combine_kernel<false>, dim3(s.T), dim3(kThreads), 0, st, topk_w, y, s.d, s.k,
-                    static_cast<const float*>(nullptr), eps, out);
+  return launch_pdl(combine_quarter_kernel, dim3(4 * s.T), dim3(128), 0, st, topk_w, y, s.d, s.k, out);
 }
 
 }  // namespace moe
