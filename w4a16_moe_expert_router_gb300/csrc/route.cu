@@ -100,44 +100,39 @@ __device__ __forceinline__ void topk_softmax_warp(const float* __restrict__ row,
 
 // Top-k of 8 tokens per CTA, then the CTA's pairs (p = t*k + r, in order) counted
 // per expert (cta_hist[cta][e]) and ranked among the CTA's earlier pairs of the
-// same expert (local_rank[p]).
+// same expert (local_rank[p]).  A token selects an expert at most once, so the
+// rank of pair (t, e) is the number of earlier tokens of the CTA that selected e:
+// one bit per token (warp) in a per-expert mask, set with an order-independent
+// atomicOr, then popcounts.
 __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                                 int32_t* __restrict__ topk_idx,
                                                                 float* __restrict__ topk_w,
                                                                 int32_t* __restrict__ cta_hist,
                                                                 int32_t* __restrict__ local_rank) {
   __shared__ int sel[kTopkWarps * kMaxTopK];
-  __shared__ int hist[kMaxExperts];
+  __shared__ unsigned emask[kMaxExperts];
   grid_dependents_launch();  // the grouping launch may set up meanwhile; it waits for this one
   grid_dependency_wait();    // logits, and the routing arrays an earlier launch may still read
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < E; e += kTopkWarps * 32) hist[e] = 0;
+  for (int e = tid; e < E; e += kTopkWarps * 32) emask[e] = 0u;
+  __syncthreads();
   const int t = blockIdx.x * kTopkWarps + warp;
   if (t < T) {
     topk_softmax_warp(logits + static_cast<size_t>(t) * E, E, k, lane, topk_idx + static_cast<size_t>(t) * k,
                       topk_w + static_cast<size_t>(t) * k, sel + warp * k);
-  } else if (lane < k) {
-    sel[warp * k + lane] = -1;
-  }
-  __syncthreads();
-  const int npairs = kTopkWarps * k;  // <= 64
-  if (warp == 0) {
-    // the CTA's pairs in rounds of 32, in pair order: a pair's rank is the count of its expert
-    // in earlier rounds plus the lower lanes of its round with the same expert
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int r0 = 0; r0 < npairs; r0 += 32) {
-      const int i = r0 + lane;
-      int e = i < npairs ? sel[i] : -1;
-      if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) e = -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      if (e >= 0) local_rank[static_cast<size_t>(blockIdx.x) * npairs + i] = hist[e] + __popc(peers & lt_mask);
-      __syncwarp();
-      if (e >= 0 && (peers & lt_mask) == 0) hist[e] += __popc(peers);
-      __syncwarp();
+    __syncwarp();
+    if (lane < k) {
+      const int e = sel[warp * k + lane];
+      if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicOr(&emask[e], 1u << warp);
     }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += kTopkWarps * 32) cta_hist[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
+  if (t < T && lane < k) {
+    const int e = sel[warp * k + lane];
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(E))
+      local_rank[static_cast<size_t>(t) * k + lane] = __popc(emask[e] & ((1u << warp) - 1u));
+  }
+  for (int e = tid; e < E; e += kTopkWarps * 32) cta_hist[static_cast<size_t>(blockIdx.x) * E + e] = __popc(emask[e]);
 }
 
 // Grouping CTA c (one per top-k CTA): thread e sums the counts of expert e over
