@@ -18,7 +18,7 @@
  *                                       gate_up_proj groups of 128 along the
  *                                       contraction dim, down_proj groups of 64
  *   [TF]  "ashhart/TensorFold pull 802", paragraph "FP64 reference": an int4 GEMM
- *         is judged against an FP64 evaluation of the same dequantised weights.
+ *         is compared with an FP64 evaluation of the same dequantised weights.
  *
  * Readings where the pages are silent (each one is listed in the design notes):
  *   - gating: softmax over the k selected logits only (no temperature, no bias);
