@@ -76,9 +76,21 @@ typedef enum {
  *   group_gate_up g1 in {32, 64, 128}, dividing d: quantisation group of gate_up_proj along d
  *   group_down    g2 in {32, 64, 128}, dividing f: quantisation group of down_proj along f
  *   activation    0 = GELU tanh form 0.5a(1+tanh(sqrt(2/pi)(a+0.044715a^3))), 1 = GELU erf form
+ *   reduction     order of the expert GEMMs' arithmetic (both give the layer within the same
+ *                 tolerance, each bit-reproducible and independent of the other tokens):
+ *                 0 = each weight dequantised to fp16, w = fp16((q - zr) s - fp16((z - zr) s)) with
+ *                     zr the integer nearest z, and multiplied into fp32 accumulators in
+ *                     contraction order;
+ *                 1 = group-factorised, the int4 GEMM order of "ashhart/TensorFold pull 802"
+ *                     (section "Contracts": partial sums per group, then the scale, then the
+ *                     bias): per quantisation group the codes are multiplied as they are into
+ *                     fp32 partial sums, then the group's scale is applied and its zero-point
+ *                     term -s z sum(x) added, group after group.  More accurate (no weight is
+ *                     rounded to fp16); work items of at most 16 tokens, so slower than 0 when
+ *                     experts get more than ~8 tokens each
  * T*k must not exceed 2^22. */
 typedef struct {
-  int32_t tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation;
+  int32_t tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation, reduction;
 } moe_w4a16_shape;
 
 /* Expert weights of one layer, in the prepared layout written by

@@ -57,7 +57,7 @@ def _shape(**kw):
 @pytest.mark.parametrize("bad", [
     dict(hidden=192), dict(hidden=64), dict(inter=96), dict(experts=0), dict(experts=257), dict(top_k=0),
     dict(top_k=9), dict(experts=4, top_k=5), dict(group_gate_up=48), dict(group_gate_up=16),
-    dict(group_down=128, inter=192), dict(activation=2), dict(tokens=-1), dict(tokens=1 << 20, top_k=8),
+    dict(group_down=128, inter=192), dict(activation=2), dict(reduction=2), dict(reduction=-1), dict(tokens=-1), dict(tokens=1 << 20, top_k=8),
 ])
 def test_invalid_shapes_rejected(bad):
     sh = _shape(**bad)

@@ -7,6 +7,7 @@ Bars (fixed by the layer's specification of this library):
                 the GPU's fp16 output against the oracle's unrounded fp64 value;
   determinism   repeated runs bit-identical.
 """
+import dataclasses
 import os
 
 import numpy as np
@@ -120,6 +121,58 @@ def test_canvas64_full_size(rt):
     _full_case(rt, synth.WORKLOADS["canvas64"])
 
 
+def _gf(wl):
+    return dataclasses.replace(wl, name=wl.name + "_gf", reduction=1)
+
+
+SHAPES = [
+    synth.WORKLOADS["tiny"],
+    synth.Workload("chunks", 300, 256, 128, 4, 2, 64, 64),
+    synth.Workload("g32", 40, 256, 192, 8, 3, 32, 32),
+    synth.Workload("g128", 33, 384, 128, 6, 2, 128, 128, activation=1),
+    synth.Workload("e256", 40, 128, 64, 256, 8, 64, 32),
+    synth.Workload("k1", 70, 256, 64, 16, 1, 128, 64),
+]
+
+
+@pytest.mark.parametrize("wl", [_gf(w) for w in SHAPES], ids=lambda w: w.name)
+def test_group_factorised_shape_variants(rt, wl):
+    """The group-factorised order (reduction = 1) on the same shapes, held to the same bars."""
+    _full_case(rt, wl, seed=5)
+
+
+def test_group_factorised_canvas256_full_size(rt):
+    _full_case(rt, _gf(synth.WORKLOADS["canvas256"]))
+
+
+def test_group_factorised_zipf1024_sampled(rt):
+    wl = _gf(synth.WORKLOADS["zipf1024"])
+    sel = np.zeros(wl.tokens, np.uint8)
+    sel[:: 8] = 1
+    _full_case(rt, wl, sel=sel)
+
+
+def test_group_factorised_is_more_accurate(rt):
+    """No weight is rounded to fp16 in the group-factorised order, so on the same
+    inputs its error against the fp64 oracle is below the per-weight order's."""
+    wl = synth.WORKLOADS["canvas64"]
+    _, rel0 = _full_case(rt, wl, seed=2)
+    _, rel1 = _full_case(rt, _gf(wl), seed=2)
+    assert rel1 < rel0, (rel1, rel0)
+
+
+@pytest.mark.parametrize("reduction", [0, 1])
+def test_batch_invariance(rt, reduction):
+    """A token's output does not depend on the other tokens of the canvas: the first
+    37 tokens alone give the rows they get inside the full 256-token canvas, bit for
+    bit (other chunkings of the experts' tokens, other token tiles)."""
+    wl = dataclasses.replace(synth.WORKLOADS["canvas256"], reduction=reduction)
+    x, lg, w = synth.make_x(wl, 4), synth.make_logits(wl, 4), synth.make_weights(wl, 4)
+    _, (full,) = _gpu_layer(rt, wl, x, lg, w)
+    _, (part,) = _gpu_layer(rt, wl, x[:37].copy(), lg[:37].copy(), w)
+    assert np.array_equal(part.view(np.uint16), full[:37].view(np.uint16))
+
+
 def test_canvas256_full_size(rt):
     _full_case(rt, synth.WORKLOADS["canvas256"])
 
@@ -137,8 +190,9 @@ def test_zipf1024_skewed_full_size(rt):
     _full_case(rt, wl, sel=sel)
 
 
-def test_canvas256_bit_identical_over_10_runs(rt):
-    wl = synth.WORKLOADS["canvas256"]
+@pytest.mark.parametrize("reduction", [0, 1])
+def test_canvas256_bit_identical_over_10_runs(rt, reduction):
+    wl = dataclasses.replace(synth.WORKLOADS["canvas256"], reduction=reduction)
     x, lg, w = synth.make_x(wl, 3), synth.make_logits(wl, 3), synth.make_weights(wl, 3)
     _, outs = _gpu_layer(rt, wl, x, lg, w, repeats=10)
     for o in outs[1:]:
@@ -180,11 +234,12 @@ def test_stack30_teacher_forced_per_layer(rt):
     assert B.moe_w4a16_read_error(buf.workspace) == B.OK
 
 
-def test_separate_calls_repeated_match_forward(rt):
+@pytest.mark.parametrize("reduction", [0, 1])
+def test_separate_calls_repeated_match_forward(rt, reduction):
     """The step-by-step entry points, each called twice in a row, give the fused
     forward's output bit for bit (every launch starts from a cleared work list)."""
     from w4a16_moe_expert_router_gb300 import binding as B
-    wl = synth.WORKLOADS["tiny"]
+    wl = dataclasses.replace(SHAPES[1], reduction=reduction)  # several token chunks per expert
     x, lg, w = synth.make_x(wl), synth.make_logits(wl), synth.make_weights(wl)
     dw = rt.upload_weights(wl, w)
     buf = rt.alloc_buffers(wl)

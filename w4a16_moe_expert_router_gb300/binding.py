@@ -39,7 +39,7 @@ class MoeW4A16Error(RuntimeError):
 
 class Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("tokens", "hidden", "inter", "experts", "top_k", "group_gate_up",
-                                              "group_down", "activation")]
+                                              "group_down", "activation", "reduction")]
 
 
 class Weights(ctypes.Structure):
@@ -107,8 +107,9 @@ def lib() -> ctypes.CDLL:
 
 # ----------------------------------------------------------------- marshalling
 
-def make_shape(tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation=0) -> Shape:
-    return Shape(tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation)
+def make_shape(tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation=0,
+               reduction=0) -> Shape:
+    return Shape(tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation, reduction)
 
 
 def _dptr(t) -> int | None:

@@ -25,7 +25,10 @@
 // zf = z - zr, and each weight is formed as w = fp16((q - zr) * s - fp16(zf * s)):
 // q - zr is exact in fp16 and the fused multiply-add rounds once.  The MMA
 // multiplies w with the fp16 activations into fp32 accumulators (16-column
-// steps in contraction order).
+// steps in contraction order).  A second instantiation of the kernel takes the
+// group-factorised order instead (shape field reduction = 1; see run_stage_gf):
+// codes as fp16 subnormals straight into the MMA, per-group fp32 partial sums,
+// scale and zero-point applied per group, items of at most 16 tokens.
 //
 // Roles of the persistent CTA (three per SM; a stage is 128 contraction columns,
 // the last one 64 when the contraction is an odd multiple of 64):
@@ -69,6 +72,7 @@ constexpr int kThreads = (1 + kMmaWarps) * 32;     // 160
 constexpr int kCtasPerSm = 3;
 constexpr int kSlots = 3;                          // stages in flight per CTA (three CTAs per SM share 227 KiB)
 constexpr int kQueue = 4;                          // item descriptors in flight per CTA
+constexpr int kChunkGf = 16;                       // tokens per work item in the group-factorised order
 constexpr int kBBoxRows = 32;                      // TMA box: 64 columns x 32 token rows
 constexpr int kBoxBytes = kBBoxRows * 128;         // 4 KiB, 128-byte swizzle
 constexpr int kBBytes = 2 * kBoxBytes;             // a stage's token tile: two boxes
@@ -134,17 +138,17 @@ __device__ __forceinline__ int expert_of(int item, const int* prefix, int E) {
 
 // Work item of one projection -> (expert, 128-row block, token chunk); the chunk
 // varies fastest, so concurrent items of a busy expert share weight blocks in L2.
-__device__ __forceinline__ void decode_item(int item, const int* prefix, const int* offs, int E, int& expert,
-                                            int& blk, int& n_cnt, int& pos0) {
+__device__ __forceinline__ void decode_item(int item, const int* prefix, const int* offs, int E, int chunk,
+                                            int& expert, int& blk, int& n_cnt, int& pos0) {
   const int e = expert_of(item, prefix, E);
   const int n_e = offs[e + 1] - offs[e];
-  const int nch = (n_e + kChunkN - 1) / kChunkN;
+  const int nch = (n_e + chunk - 1) / chunk;
   const int r = item - prefix[e];
   const int c = r % nch;
   expert = e;
   blk = r / nch;
-  n_cnt = min(kChunkN, n_e - kChunkN * c);
-  pos0 = offs[e] + kChunkN * c;
+  n_cnt = min(chunk, n_e - chunk * c);
+  pos0 = offs[e] + chunk * c;
 }
 
 constexpr uint64_t kDepWaitNs = 2000000000ull;  // bound of the wait for an expert's gate_up outputs
@@ -201,6 +205,52 @@ __device__ __forceinline__ void dequant_frag(uint32_t w, const DqRows& k, uint32
   a[1] = h2_bits(__hfma2(__hsub2(bits_h2(and_or(w, 0x00f000f0u, 0x54005400u)), k.zb_hi), k.s_hi, k.c_hi));
   a[2] = h2_bits(__hfma2(__hsub2(bits_h2(and_or(w8, 0x000f000fu, 0x64006400u)), k.zb_lo), k.s_lo, k.c_lo));
   a[3] = h2_bits(__hfma2(__hsub2(bits_h2(and_or(w8, 0x00f000f0u, 0x54005400u)), k.zb_hi), k.s_hi, k.c_hi));
+}
+
+// Group-factorised order ("ashhart/TensorFold pull 802", section "Contracts":
+// partial sums per group, then the scale, then the bias): the codes go to the MMA
+// as they are, as fp16 subnormals, and each group's scale and zero-point are
+// applied once per group to fp32 partial sums:
+//   sum_k x_k (q_k - z) s = s * sum_k x_k q_k - s z * sum_k x_k   (k over one group).
+// One word of codes -> the A fragment by masks alone: rows g hold q * 2^-24, rows
+// g + 8 hold 16 q * 2^-24 (their nibbles sit four bits higher and stay there).
+// Products of fp16 values are exact in the fp32 accumulators.
+__device__ __forceinline__ void code_frag(uint32_t w, uint32_t (&a)[4]) {
+  const uint32_t w8 = w >> 8;
+  a[0] = w & 0x000f000fu;
+  a[1] = w & 0x00f000f0u;
+  a[2] = w8 & 0x000f000fu;
+  a[3] = w8 & 0x00f000f0u;
+}
+
+// Per-group fp32 constants of one thread's rows g and g + 8 (v.x, v.y as in dq_rows),
+// in the units of the partial sums: s for rows g, s / 16 for rows g + 8, and -s z
+// for the sum of the activations (products of two fp16 values: exact).
+struct GfRows {
+  float s_lo, z_lo, s_hi, z_hi;
+};
+__device__ __forceinline__ GfRows gf_rows(uint32_t vx, uint32_t vy) {
+  const float2 a = __half22float2(bits_h2(vx)), b = __half22float2(bits_h2(vy));
+  GfRows k;
+  k.s_lo = a.x;
+  k.z_lo = -a.x * a.y;
+  k.s_hi = b.x * 0.0625f;
+  k.z_hi = -b.x * b.y;
+  return k;
+}
+
+// D = A * B + (Z ? 0 : D)
+template <bool Z>
+__device__ __forceinline__ void mma_acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if (Z) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+  } else {
+    mma_f16_16816(d, a, b0, b1);
+  }
 }
 
 __device__ __forceinline__ float gelu(float a, int act) {
@@ -342,9 +392,108 @@ __device__ __forceinline__ bool run_stage(const MmArgs& a, MmHeader& H, volatile
   return true;
 }
 
+// One stage in the group-factorised form (items of at most two token tiles): per
+// group, the MMAs of both strips into partial sums that start at zero, and the
+// activation sums of the item's 16 token rows, then
+// tot += s * partial - s z * sum (two fused multiply-adds per accumulator).  tot is
+// in units of 2^-24.  The sums take one more MMA per 16-column step with the roles
+// swapped: the token fragments the step already holds (tokens 0-7 and 8-15 at its
+// two 8-column halves) form the m16k16 A fragment {b0, b2, b1, b3}, times a B
+// fragment of 2^-24, so that row m of the result is token m's sum; four shuffles
+// move those into the accumulators' token columns.
+template <int NT, int G, int KK>
+__device__ __forceinline__ bool run_stage_gf(const MmArgs& a, MmHeader& H, volatile int* abort,
+                                             float (&tot)[2][NT][4], int& slot, uint32_t& phase, uint32_t ring_s,
+                                             const uint32_t (&loff)[4], int sw, int lane) {
+  static_assert(NT == 1 || NT == 2, "group-factorised items have at most 16 tokens");
+  constexpr int NG = (16 * KK) / (G < 16 * KK ? G : 16 * KK);
+  constexpr int kStepsPerGroup = KK / NG;
+  constexpr int kStripBytes = KK * 128 + kSzBytesW * NG;
+  constexpr uint32_t kUnit = 0x00010001u;  // 2^-24 in both halves
+  if (!warp_wait(smem_addr(&H.slot_full[slot]), phase, a, abort)) return false;
+  const uint32_t sl = ring_s + slot * kSlotBytes;
+  const uint32_t wseg = sl + kBBytes + 2 * sw * kStripBytes;
+  const uint32_t caddr = wseg + kSzBytesW * NG + lane * 16;
+  uint32_t szw[2][2 * NG];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t szaddr = wseg + h * kStripBytes + (lane >> 2) * (8 * NG);
+    if (NG == 1) {
+      asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(szw[h][0]), "=r"(szw[h][1]) : "r"(szaddr));
+    } else {
+#pragma unroll
+      for (int q = 0; q < NG / 2; ++q)
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(szw[h][4 * q]), "=r"(szw[h][4 * q + 1]), "=r"(szw[h][4 * q + 2]), "=r"(szw[h][4 * q + 3])
+                     : "r"(szaddr + 16 * q));
+    }
+  }
+  uint32_t words[2][4];
+#pragma unroll
+  for (int j = 0; j < NG; ++j) {
+    float part[2][NT][4], rs[4];  // rs: sums of token rows g (0, 1) and g + 8 (2, 3)
+#pragma unroll
+    for (int st = 0; st < kStepsPerGroup; ++st) {
+      const int kk = j * kStepsPerGroup + st;
+      if (kk % 4 == 0)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(words[h][0]), "=r"(words[h][1]), "=r"(words[h][2]), "=r"(words[h][3])
+                       : "r"(caddr + h * kStripBytes + (kk / 4) * 512));
+      uint32_t af[2][4];
+      code_frag(words[0][kk % 4], af[0]);
+      code_frag(words[1][kk % 4], af[1]);
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4(sl + (kk / 4) * kBoxBytes + loff[kk % 4], b0, b1, b2, b3);
+      const uint32_t tok[4] = {b0, b2, b1, b3};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (st == 0) {
+          mma_acc<true>(part[h][0], af[h], b0, b1);
+          if (NT > 1) mma_acc<true>(part[h][NT - 1], af[h], b2, b3);
+        } else {
+          mma_acc<false>(part[h][0], af[h], b0, b1);
+          if (NT > 1) mma_acc<false>(part[h][NT - 1], af[h], b2, b3);
+        }
+      }
+      if (st == 0) mma_acc<true>(rs, tok, kUnit, kUnit);
+      else mma_acc<false>(rs, tok, kUnit, kUnit);
+    }
+    // token column n of tile u is row 8 u + n of rs, held by lanes 4 n .. 4 n + 3
+    const int src = 8 * (lane & 3);
+    float xs[NT][2];
+    xs[0][0] = __shfl_sync(0xffffffffu, rs[0], src);
+    xs[0][1] = __shfl_sync(0xffffffffu, rs[0], src + 4);
+    if (NT > 1) {
+      xs[NT - 1][0] = __shfl_sync(0xffffffffu, rs[2], src);
+      xs[NT - 1][1] = __shfl_sync(0xffffffffu, rs[2], src + 4);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const GfRows k = gf_rows(szw[h][2 * j], szw[h][2 * j + 1]);
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        float(&t)[4] = tot[h][u];
+        t[0] = fmaf(k.s_lo, part[h][u][0], fmaf(k.z_lo, xs[u][0], t[0]));
+        t[1] = fmaf(k.s_lo, part[h][u][1], fmaf(k.z_lo, xs[u][1], t[1]));
+        t[2] = fmaf(k.s_hi, part[h][u][2], fmaf(k.z_hi, xs[u][0], t[2]));
+        t[3] = fmaf(k.s_hi, part[h][u][3], fmaf(k.z_hi, xs[u][1], t[3]));
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_addr(&H.slot_empty[slot]));
+  if (++slot == kSlots) {
+    slot = 0;
+    phase ^= 1u;
+  }
+  return true;
+}
+
 // One item of one compute warp: every stage of the contraction, then the epilogue.
 // Returns false if a wait gave up.
-template <int NT, int G>
+template <int NT, int G, bool GF>
 __device__ __forceinline__ bool run_item(const MmArgs& a, MmHeader& H, volatile int* abort, const ItemView& v,
                                          int& slot, uint32_t& phase, uint32_t ring_s, const uint32_t (&loff)[4],
                                          int sw, int lane) {
@@ -357,10 +506,26 @@ __device__ __forceinline__ bool run_item(const MmArgs& a, MmHeader& H, volatile 
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[h][nt][j] = 0.f;
   const int K = a.p[v.pj].K;
-  for (int c0 = 0; c0 + kStageCols <= K; c0 += kStageCols)
-    if (!run_stage<NT, G, 8>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
-  if (G < 128 && (K % kStageCols) != 0)  // the last 64 columns
-    if (!run_stage<NT, (G < 64 ? G : 64), 4>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
+  constexpr int G4 = G < 64 ? G : 64;  // groups of the last 64 columns
+  if constexpr (GF) {
+    for (int c0 = 0; c0 + kStageCols <= K; c0 += kStageCols)
+      if (!run_stage_gf<NT, G, 8>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
+    if (G < 128 && (K % kStageCols) != 0)
+      if (!run_stage_gf<NT, G4, 4>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
+  } else {
+    for (int c0 = 0; c0 + kStageCols <= K; c0 += kStageCols)
+      if (!run_stage<NT, G, 8>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
+    if (G < 128 && (K % kStageCols) != 0)  // the last 64 columns
+      if (!run_stage<NT, G4, 4>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
+  }
+  if constexpr (GF) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[h][nt][j] *= 16777216.f;  // 2^24: back from the partial sums' units
+  }
   // ------------------------------------------------------------------ epilogue
   if (v.pj == 0) {
     // strip s: rows gq gate j, gq + 8 up j, with j = 64 * blk + 8 * s + gq
@@ -409,21 +574,29 @@ __device__ __forceinline__ bool run_item(const MmArgs& a, MmHeader& H, volatile 
   return true;
 }
 
-template <int G>
+template <int G, bool GF>
 __device__ __forceinline__ bool run_item_g(const MmArgs& a, MmHeader& H, volatile int* abort, const ItemView& v,
                                            int& slot, uint32_t& phase, uint32_t ring_s, const uint32_t (&loff)[4],
                                            int sw, int lane) {
-  switch ((v.n_cnt + 7) / 8) {
-    case 1: return run_item<1, G>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
-    case 2: return run_item<2, G>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
-    case 3: return run_item<3, G>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
-    default: return run_item<4, G>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+  const int nt = (v.n_cnt + 7) / 8;
+  if constexpr (GF)  // items of at most kChunkGf tokens
+    return nt == 1 ? run_item<1, G, true>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
+                   : run_item<2, G, true>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+  switch (nt) {
+    case 1: return run_item<1, G, false>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+    case 2: return run_item<2, G, false>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+    case 3: return run_item<3, G, false>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+    default: return run_item<4, G, false>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
   }
 }
 
+// GF: the group-factorised reduction order (its own instantiation, so that each
+// order gets its own register allocation).
+template <bool GF>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     expert_gemm_mma_kernel(const MmArgs a, const __grid_constant__ CUtensorMap map_x,
                            const __grid_constant__ CUtensorMap map_h) {
+  constexpr int kChunk = GF ? kChunkGf : kChunkN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   MmHeader& H = *reinterpret_cast<MmHeader*>(smem);
@@ -454,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       for (int j = 0; j < 8; ++j) {
         const int e = lane * 8 + j;
         loc[j] = sum;
-        if (e < a.E) sum += nb * ((a.offsets[e + 1] - a.offsets[e] + kChunkN - 1) / kChunkN);
+        if (e < a.E) sum += nb * ((a.offsets[e + 1] - a.offsets[e] + kChunk - 1) / kChunk);
       }
       int incl = sum;
 #pragma unroll
@@ -495,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (lane == 0 && !done) next = atomicAdd(a.counter, 1);
       const int pj = (a.first == 0 && item < total0) ? 0 : 1;
       int e = 0, blk = 0, n_cnt = 0, pos0 = 0;
-      if (!done) decode_item(pj == 0 ? item : item - total0, H.prefix[pj], H.offs, a.E, e, blk, n_cnt, pos0);
+      if (!done) decode_item(pj == 0 ? item : item - total0, H.prefix[pj], H.offs, a.E, kChunk, e, blk, n_cnt, pos0);
       ok = warp_wait(smem_addr(&H.item_empty[i % kQueue]), ((i / kQueue) & 1) ^ 1, a, abort);
       if (!ok) break;
       if (lane == 0) {
@@ -510,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // a down item reads the h rows of its expert: wait until every gate_up warp of the
         // expert has written them
         if (lane == 0) {
-          const int need = kMmaWarps * a.p[0].nblocks * ((H.offs[e + 1] - H.offs[e] + kChunkN - 1) / kChunkN);
+          const int need = kMmaWarps * a.p[0].nblocks * ((H.offs[e + 1] - H.offs[e] + kChunk - 1) / kChunk);
           ok = wait_count(a.gu_done + e, need, a.err, abort, kDepWaitNs);
           // the TMA loads below read those rows through the async proxy
           asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -566,9 +739,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (!warp_wait(smem_addr(&H.item_full[i % kQueue]), (i / kQueue) & 1, a, abort)) break;
       ItemView v;
       if (!read_item(H, i, a, v)) break;
-      const bool ok = v.g == 32   ? run_item_g<32>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
-                      : v.g == 64 ? run_item_g<64>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
-                                  : run_item_g<128>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+      const bool ok = v.g == 32   ? run_item_g<32, GF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
+                      : v.g == 64 ? run_item_g<64, GF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
+                                  : run_item_g<128, GF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&H.item_empty[i % kQueue]));
@@ -663,11 +836,13 @@ bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
 }  // namespace
 
 cudaError_t init_gemm_kernels(int* blocks_per_sm) {
-  const void* fn = reinterpret_cast<const void*>(expert_gemm_mma_kernel);
-  cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (err != cudaSuccess) return err;
-  err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (err != cudaSuccess) return err;
+  for (const void* fn : {reinterpret_cast<const void*>(expert_gemm_mma_kernel<false>),
+                         reinterpret_cast<const void*>(expert_gemm_mma_kernel<true>)}) {
+    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (err != cudaSuccess) return err;
+  }
   *blocks_per_sm = kCtasPerSm;
   return cudaSuccess;
 }
@@ -717,7 +892,8 @@ cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, cons
   }
   CUtensorMap map_x, map_h;
   if (!make_row_map(&map_x, ws.xs, P, s.d) || !make_row_map(&map_h, ws.h, P, s.f)) return cudaErrorInvalidValue;
-  return launch_pdl(expert_gemm_mma_kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, a, map_x, map_h);
+  return s.red ? launch_pdl(expert_gemm_mma_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, st, a, map_x, map_h)
+               : launch_pdl(expert_gemm_mma_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, st, a, map_x, map_h);
 }
 
 }  // namespace moe

@@ -45,6 +45,7 @@ class Workload:
     zipf_s: float = 0.0        # 0 = unbiased N(0,1) logits
     rmsnorm: bool = False      # fp32 RMSNorm after every layer (gamma ~ N(1, 0.1))
     activation: int = 0        # 0 = GELU tanh form, 1 = GELU erf form
+    reduction: int = 0         # 0 = each weight dequantised, 1 = group-factorised expert GEMMs
 
     def weight_bytes_per_expert(self) -> int:
         """Packed nibbles plus fp16 scale and zero of both projections."""
