@@ -1,12 +1,13 @@
-"""ctypes loader for the fp64 CPU oracle in ``moe_oracle.c``.
+"""ctypes loader for the CPU oracle: ``moe_oracle.c`` (the MoE expert layer, fp64)
+and ``sampler_oracle.c`` (the per-step sampler: entropy, Gumbel-max, acceptance).
 
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
 and by the CPU-baseline leg of ``bench.py``.  The product path (the package
 ``w4a16_moe_expert_router_gb300``) never imports this module, and this module
 never imports the product package.
 
-Every function here is marshalling only; the arithmetic is in ``moe_oracle.c``,
-which cites the passages of the pages it follows.
+Every function here is marshalling only; the arithmetic is in the two C files,
+which cite the passages of the pages they follow.
 """
 from __future__ import annotations
 
@@ -18,7 +19,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "moe_oracle.c")
+_SRCS = [os.path.join(_HERE, "moe_oracle.c"), os.path.join(_HERE, "sampler_oracle.c")]
 _LIB_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_LIB_DIR, "libmoe_oracle.so")
 _lock = threading.Lock()
@@ -30,10 +31,10 @@ OK, ERR_SHAPE, ERR_NONFINITE, ERR_ALLOC = 0, 1, 2, 3
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (plain C11, no fp contraction, no fast-math)."""
     os.makedirs(_LIB_DIR, exist_ok=True)
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(os.path.getmtime(f) for f in _SRCS):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fPIC", "-shared",
-                               "-pthread", "-o", tmp, _SRC, "-lm"])
+                               "-pthread", "-o", tmp, *_SRCS, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -71,6 +72,15 @@ def lib():
                                              dbl, vp, ctypes.c_int, ctypes.c_int, vp]
             L.oracle_moe_forward_dense.argtypes = [ctypes.POINTER(_Shape), vp, vp, vp,
                                                    ctypes.POINTER(_Weights), vp]
+            L.oracle_philox4x32_10.argtypes = [vp, vp, vp]
+            L.oracle_log_f32.argtypes = [ctypes.c_float]
+            L.oracle_log_f32.restype = ctypes.c_float
+            L.oracle_gumbel_key.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_uint32]
+            L.oracle_gumbel_key.restype = ctypes.c_float
+            L.oracle_sample.argtypes = [i32, i64, vp, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32,
+                                        ctypes.c_int, vp, vp, vp]
+            L.oracle_accept_entropy.argtypes = [i32, vp, vp, ctypes.c_float, vp]
+            L.oracle_accept_confidence.argtypes = [i32, vp, vp, ctypes.c_float, vp]
             _lib = L
     return _lib
 
@@ -196,3 +206,59 @@ def forward_dense(x_bits: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, 
     if st != OK:
         raise ValueError(f"oracle_moe_forward_dense status {st}")
     return out
+
+
+# ------------------------------------------------------------------ sampler
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    """Philox4x32-10 of one counter (4 words) under one key (2 words)."""
+    c = np.ascontiguousarray(ctr, np.uint32)
+    k = np.ascontiguousarray(key, np.uint32)
+    out = np.zeros(4, np.uint32)
+    lib().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def log_f32(x: float) -> float:
+    """The fp32 natural log the Gumbel keys are defined with."""
+    return float(lib().oracle_log_f32(ctypes.c_float(x)))
+
+
+def gumbel_key(logit: float, inv_temp: float, word: int) -> float:
+    return float(lib().oracle_gumbel_key(ctypes.c_float(logit), ctypes.c_float(inv_temp), ctypes.c_uint32(word)))
+
+
+def sample(logits: np.ndarray, inv_temp: float, seed: int, step: int, nthreads: int = 1):
+    """Gumbel-max tokens (int32 [P]) and fp64 entropy and top-1 probability [P] of softmax(logits * inv_temp)."""
+    lg = _c(logits, np.float32)
+    P, V = lg.shape
+    tok = np.zeros(P, np.int32)
+    ent = np.zeros(P, np.float64)
+    pm = np.zeros(P, np.float64)
+    st = lib().oracle_sample(P, V, _ptr(lg), float(inv_temp), int(seed), int(step), int(nthreads), _ptr(tok),
+                             _ptr(ent), _ptr(pm))
+    if st != OK:
+        raise ValueError(f"oracle_sample status {st}")
+    return tok, ent, pm
+
+
+def accept_entropy(entropy: np.ndarray, revealed: np.ndarray, bound: float) -> np.ndarray:
+    """Entropy-bound acceptance (uint8 [P]) decided on fp32 entropies."""
+    h = _c(entropy, np.float32)
+    rv = _c(revealed, np.uint8)
+    acc = np.zeros(h.shape[0], np.uint8)
+    st = lib().oracle_accept_entropy(h.shape[0], _ptr(h), _ptr(rv), float(bound), _ptr(acc))
+    if st != OK:
+        raise ValueError(f"oracle_accept_entropy status {st}")
+    return acc
+
+
+def accept_confidence(pmax: np.ndarray, revealed: np.ndarray, threshold: float) -> np.ndarray:
+    """Confidence-threshold acceptance (uint8 [P]) decided on fp32 top-1 probabilities."""
+    pm = _c(pmax, np.float32)
+    rv = _c(revealed, np.uint8)
+    acc = np.zeros(pm.shape[0], np.uint8)
+    st = lib().oracle_accept_confidence(pm.shape[0], _ptr(pm), _ptr(rv), float(threshold), _ptr(acc))
+    if st != OK:
+        raise ValueError(f"oracle_accept_confidence status {st}")
+    return acc

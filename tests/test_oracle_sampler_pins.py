@@ -1,0 +1,220 @@
+"""Pins of the sampler oracle (oracle/sampler_oracle.c) to things other than itself:
+libm's logarithm, closed forms of the entropy, the distribution Gumbel-max must
+sample, generator statistics, and the page's own formula of the entropy-bound rule.
+
+Sources: "srswti/axe-diffusion-ksl-xe" model card ("the kernels we built": entropy in
+one streaming pass, Gumbel-max instead of softmax + multinomial); "lablup/mlxcel
+block-diffusion docs" ("Samplers": the entropy-bound rule, the mlx-vlm formula
+(cumsum - cummax) <= bound, at least one accepted; the confidence-threshold rule);
+Salmon et al., SC'11 (Philox4x32-10).
+
+The bit pattern of Philox4x32-10 itself is pinned only by statistics here and by the
+bit-exact agreement of the GPU path's independent implementation with this one.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def _ulp(v: float) -> float:
+    return float(np.spacing(np.float32(abs(v))))
+
+
+# ------------------------------------------------------------------ log_f32
+
+def test_log_f32_against_libm_over_the_noise_domain():
+    """Within 2.5 fp32 ulps of the exact logarithm on the two ranges the Gumbel noise
+    uses (U in [2^-24, 1), E = -ln U in (0, 17]) and across the exponent range (the
+    roundings of the quotient, the Horner steps and the product give ~2 ulps near
+    x = 1; a wrong series coefficient costs 5 or more)."""
+    rng = np.random.default_rng(0)
+    xs = np.concatenate([
+        ((np.arange(0, 1 << 23, 97) + 0.5) * 2.0 ** -23),          # the U grid itself
+        1.0 - np.arange(1, 4096) * 2.0 ** -24,                      # just below 1
+        1.0 + np.arange(1, 4096) * 2.0 ** -23,                      # just above 1
+        rng.uniform(1e-7, 17.0, 20000),
+        2.0 ** rng.uniform(-120, 120, 20000),
+    ]).astype(np.float32)
+    worst = 0.0
+    for x in xs[:: 7]:
+        got = oracle.log_f32(float(x))
+        want = math.log(float(x))
+        if want == 0.0:
+            assert got == 0.0
+            continue
+        worst = max(worst, abs(got - want) / _ulp(want))
+    assert worst <= 2.5, worst
+
+
+def test_log_f32_special_values():
+    assert oracle.log_f32(1.0) == 0.0
+    for k in range(-30, 31):
+        want = k * math.log(2.0)
+        got = oracle.log_f32(2.0 ** k)
+        assert abs(got - want) <= (_ulp(want) if k else 0.0)
+
+
+# ------------------------------------------------------------------ Philox
+
+def test_philox_words_are_uniform_and_counters_avalanche():
+    """Counter-based: the same (counter, key) gives the same words; across counters the
+    words are uniform (chi-square on the top 4 bits) and flipping one counter or key
+    bit flips about half of the 128 output bits."""
+    key = np.array([0x12345678, 0x9abcdef0], np.uint32)
+    a = oracle.philox4x32_10([5, 6, 7, 8], key)
+    assert np.array_equal(a, oracle.philox4x32_10([5, 6, 7, 8], key))
+    words = np.concatenate([oracle.philox4x32_10([i, 3, 1, 0], key) for i in range(4096)])
+    counts = np.bincount(words >> 28, minlength=16)
+    exp = len(words) / 16
+    chi2 = float(((counts - exp) ** 2 / exp).sum())
+    assert chi2 < 37.7  # chi-square, 15 degrees of freedom, p = 0.001
+    rng = np.random.default_rng(1)
+    flips = []
+    for _ in range(200):
+        c = rng.integers(0, 2 ** 32, 4, dtype=np.uint64).astype(np.uint32)
+        k = rng.integers(0, 2 ** 32, 2, dtype=np.uint64).astype(np.uint32)
+        base = oracle.philox4x32_10(c, k)
+        bit = int(rng.integers(0, 192))
+        c2, k2 = c.copy(), k.copy()
+        if bit < 128:
+            c2[bit // 32] ^= np.uint32(1 << (bit % 32))
+        else:
+            k2[(bit - 128) // 32] ^= np.uint32(1 << (bit % 32))
+        d = oracle.philox4x32_10(c2, k2) ^ base
+        flips.append(sum(bin(int(w)).count("1") for w in d))
+    assert 60 <= np.mean(flips) <= 68
+
+
+# ------------------------------------------------------------------ entropy
+
+def test_entropy_of_uniform_logits_is_log_v():
+    V = 4096
+    lg = np.full((3, V), 0.25, np.float32)
+    _, ent, pm = oracle.sample(lg, 1.0, 7, 0)
+    assert np.allclose(ent, math.log(V), rtol=0, atol=1e-12)
+    assert np.allclose(pm, 1.0 / V, rtol=1e-14)
+
+
+def test_entropy_of_a_two_point_distribution():
+    """Two logits a, b and the rest so low that exp underflows: H is the binary entropy of sigmoid(a - b)."""
+    V = 64
+    lg = np.full((1, V), -1e5, np.float32)
+    lg[0, 10], lg[0, 40] = 1.5, -0.25
+    _, ent, pm = oracle.sample(lg, 1.0, 1, 0)
+    p = 1.0 / (1.0 + math.exp(-(1.5 + 0.25)))
+    assert abs(ent[0] - (-p * math.log(p) - (1 - p) * math.log(1 - p))) < 1e-12
+    assert abs(pm[0] - p) < 1e-12
+
+
+def test_entropy_and_confidence_against_scipy():
+    scipy_special = pytest.importorskip("scipy.special")
+    scipy_stats = pytest.importorskip("scipy.stats")
+    rng = np.random.default_rng(6)
+    lg = (rng.standard_normal((5, 3000)) * 3).astype(np.float32)
+    _, ent, pm = oracle.sample(lg, 0.7, 1, 0)
+    p = scipy_special.softmax(lg.astype(np.float64) * np.float64(np.float32(0.7)), axis=1)
+    assert np.allclose(ent, scipy_stats.entropy(p, axis=1), rtol=1e-12, atol=1e-12)
+    assert np.allclose(pm, p.max(1), rtol=1e-12)
+
+
+def test_temperature_scales_the_logits():
+    rng = np.random.default_rng(2)
+    lg = rng.standard_normal((2, 512)).astype(np.float32)
+    _, e1, p1 = oracle.sample(lg, 2.0, 3, 0)
+    _, e2, p2 = oracle.sample((lg * 2).astype(np.float32), 1.0, 3, 0)
+    assert np.allclose(e1, e2, rtol=0, atol=1e-12) and np.allclose(p1, p2, rtol=1e-12)
+
+
+# ------------------------------------------------------------------ Gumbel-max
+
+@pytest.mark.parametrize("inv_temp", [1.0, 0.5])
+def test_gumbel_max_samples_the_softmax(inv_temp):
+    """The tokens of 40000 positions with the same logits (each position its own
+    counters) follow softmax(logits * inv_temp): chi-square at p = 1e-4."""
+    base = np.array([0.0, 1.0, 2.0, -1.0, 0.5, 3.0, -2.0, 1.5], np.float32)
+    P = 40000
+    tok, _, _ = oracle.sample(np.tile(base, (P, 1)), inv_temp, 11, 4, nthreads=8)
+    p = np.exp(base.astype(np.float64) * inv_temp)
+    p /= p.sum()
+    counts = np.bincount(tok, minlength=8)
+    chi2 = float(((counts - P * p) ** 2 / (P * p)).sum())
+    assert chi2 < 29.9  # chi-square, 7 degrees of freedom, p = 1e-4
+
+
+def test_gumbel_key_matches_the_definition_in_fp64():
+    """key = t + G with G = -ln(-ln U): the fp32 definition stays within a few ulps of
+    the same steps taken in fp64."""
+    rng = np.random.default_rng(3)
+    for w in rng.integers(0, 2 ** 32, 2000, dtype=np.uint64):
+        w = int(w)
+        u = ((w >> 9) + 0.5) * 2.0 ** -23
+        want = 0.75 * 1.25 - math.log(-math.log(u))
+        got = oracle.gumbel_key(0.75, 1.25, w)
+        assert abs(got - want) <= 8 * _ulp(want) + 1e-6
+
+
+def test_dominant_logit_wins_and_seeds_change_draws():
+    lg = np.zeros((4, 256), np.float32)
+    lg[:, 77] = 60.0  # exp(60) outweighs any Gumbel noise the 23-bit uniforms can give (G <= 16.7)
+    tok, _, _ = oracle.sample(lg, 1.0, 5, 9)
+    assert np.all(tok == 77)
+    rng = np.random.default_rng(4)
+    lg = rng.standard_normal((64, 1024)).astype(np.float32)
+    t1, _, _ = oracle.sample(lg, 1.0, 1, 0)
+    t2, _, _ = oracle.sample(lg, 1.0, 2, 0)
+    t3, _, _ = oracle.sample(lg, 1.0, 1, 1)
+    assert np.array_equal(t1, oracle.sample(lg, 1.0, 1, 0)[0])
+    assert (t1 != t2).mean() > 0.5 and (t1 != t3).mean() > 0.5
+
+
+# ------------------------------------------------------------------ acceptance
+
+def _mlx_vlm_rule(ent, revealed, bound):
+    """The page's formula, restated with numpy: sort the unrevealed entropies ascending
+    (stable, so ties keep position order), mask = (cumsum - cummax) <= bound in fp32,
+    and the first sorted position always."""
+    idx = np.nonzero(revealed == 0)[0]
+    order = idx[np.argsort(ent[idx], kind="stable")]
+    h = ent[order].astype(np.float32)
+    cs = np.cumsum(h, dtype=np.float32)
+    cm = np.maximum.accumulate(h)
+    mask = (cs - cm) <= np.float32(bound)
+    if len(mask):
+        mask[0] = True
+    out = np.zeros(len(ent), np.uint8)
+    out[order[mask]] = 1
+    return out
+
+
+def test_entropy_bound_worked_example():
+    ent = np.array([0.5, 0.1, 0.3, 0.2], np.float32)
+    acc = oracle.accept_entropy(ent, np.zeros(4, np.uint8), 0.35)
+    # sorted 0.1 (1), 0.2 (3), 0.3 (2), 0.5 (0): sums before each 0, 0.1, 0.3, 0.6
+    assert acc.tolist() == [0, 1, 1, 1]
+    assert oracle.accept_entropy(ent, np.zeros(4, np.uint8), -1.0).tolist() == [0, 1, 0, 0]
+    assert oracle.accept_entropy(ent, np.array([0, 1, 0, 0], np.uint8), 0.25).tolist() == [0, 0, 1, 1]
+    assert oracle.accept_entropy(ent, np.ones(4, np.uint8), 10.0).tolist() == [0, 0, 0, 0]
+
+
+def test_entropy_bound_equals_the_mlx_vlm_formula():
+    rng = np.random.default_rng(5)
+    for trial in range(50):
+        P = int(rng.integers(1, 400))
+        ent = (rng.gamma(1.0, 1.0, P) * rng.choice([1.0, 0.01])).astype(np.float32)
+        ent[rng.random(P) < 0.1] = ent[0]  # ties
+        revealed = (rng.random(P) < 0.3).astype(np.uint8)
+        bound = float(rng.uniform(-0.5, 5.0))
+        assert np.array_equal(oracle.accept_entropy(ent, revealed, bound), _mlx_vlm_rule(ent, revealed, bound))
+
+
+def test_confidence_threshold_rule():
+    pm = np.array([0.95, 0.5, 0.91, 0.99, 0.2], np.float32)
+    rv = np.array([0, 0, 0, 1, 0], np.uint8)
+    assert oracle.accept_confidence(pm, rv, 0.9).tolist() == [1, 0, 1, 0, 0]
+    # none above: the most confident unrevealed position, ties to the lower position
+    assert oracle.accept_confidence(np.array([0.3, 0.6, 0.6, 0.99], np.float32), np.array([0, 0, 0, 1], np.uint8),
+                                    0.9).tolist() == [0, 1, 0, 0]
+    assert oracle.accept_confidence(pm, np.ones(5, np.uint8), 0.9).tolist() == [0, 0, 0, 0, 0]
