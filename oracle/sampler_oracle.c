@@ -28,7 +28,8 @@
  *     entropy is that distribution's, H = -sum_v p_v ln p_v (natural log); the
  *     confidence of a position is max_v p_v;
  *   - Gumbel-max: token = argmax_v (t_v + G_v), G_v = -ln(-ln U_v), ties to the lower
- *     index; U_v = ((x >> 9) + 1/2) 2^-23 from the 32-bit word x that Philox4x32-10
+ *     index; U_v = ((x & 0x7fffff) + 1/2) 2^-23 from the low 23 bits of the 32-bit
+ *     word x that Philox4x32-10
  *     gives for element v: counter (v / 4, position, step, 0), key (seed low, seed
  *     high), word v % 4;
  *   - the key t_v + G_v decides an integer, so it is defined in fp32 with one IEEE
@@ -119,10 +120,10 @@ float oracle_log_f32(float x) {
   return fmaf(ef, 0.693145751953125f, fmaf(ef, 1.42860677e-06f, lnm));
 }
 
-/* The Gumbel-max key of one element: U from the word's upper 23 bits (exact),
+/* The Gumbel-max key of one element: U from the word's low 23 bits (exact),
  * E = -ln U, G = -ln E, key = fmaf(logit, inv_temp, G). */
 float oracle_gumbel_key(float logit, float inv_temp, uint32_t word) {
-  const float u = ((float)(word >> 9) + 0.5f) * 0x1p-23f;
+  const float u = ((float)(word & 0x007fffffu) + 0.5f) * 0x1p-23f;
   const float e = -oracle_log_f32(u);
   const float g = -oracle_log_f32(e);
   return fmaf(logit, inv_temp, g);

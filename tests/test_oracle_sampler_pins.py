@@ -150,7 +150,7 @@ def test_gumbel_key_matches_the_definition_in_fp64():
     rng = np.random.default_rng(3)
     for w in rng.integers(0, 2 ** 32, 2000, dtype=np.uint64):
         w = int(w)
-        u = ((w >> 9) + 0.5) * 2.0 ** -23
+        u = ((w & 0x7FFFFF) + 0.5) * 2.0 ** -23
         want = 0.75 * 1.25 - math.log(-math.log(u))
         got = oracle.gumbel_key(0.75, 1.25, w)
         assert abs(got - want) <= 8 * _ulp(want) + 1e-6
