@@ -7,6 +7,11 @@ gated GELU, the grouped down GEMM and the fixed-order combine, all through the
 library's C ABI on device-resident inputs.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload canvas256] [--impl ours|reference]
+  python bench.py --sampler [--steps K] [--warmup W]
+
+`--sampler` times the per-step sampler instead (entropy, Gumbel-max token and
+acceptance over the fp32 logits of a 256-position canvas with a 262,144-token
+vocabulary: 268 MB per step) and prints its own JSON line.
 
 Under torchrun every rank runs its own canvas on its own GPU (independent
 problems, no collective on the data path): weak scaling; value = tokens of all
@@ -46,6 +51,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=2000)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sampler", action="store_true", help="time the per-step sampler instead of the layer")
     return p.parse_args(argv)
 
 
@@ -437,8 +443,111 @@ def run_reference(args, rank, world):
     }
 
 
+SAMPLER_METRIC = "sampler steps/s (256 positions x 262,144 vocabulary fp32 logits); achieved HBM GB/s vs GB300 peak"
+SAMPLER_PROFILE = os.path.join(ROOT, "profiles", "sampler_pass_p256_v262144.txt")
+SAMPLER_SRC = os.path.join(ROOT, "w4a16_moe_expert_router_gb300", "csrc", "sampler.cu")
+
+
+def run_sampler(args):
+    """K sampler calls on device-resident logits (two 268 MB copies alternate, each
+    larger than L2), CUDA events on the launching stream; then the same call end to
+    end with the logits copied in from pinned host memory and the outputs read back."""
+    import numpy as np
+    import torch
+    from w4a16_moe_expert_router_gb300 import binding as B
+    from w4a16_moe_expert_router_gb300 import build as libbuild
+    libbuild.build()
+    P, V, seed = 256, 262144, 1234
+    steps, warmup = min(args.steps, 2000), max(3, min(args.warmup, 20))
+    rng = np.random.default_rng(0)
+    host = [(rng.standard_normal((P, V), dtype=np.float32) * 3.0) for _ in range(2)]
+    dev = [torch.from_numpy(h).cuda() for h in host]
+    revealed = torch.zeros(P, dtype=torch.uint8, device="cuda")
+    tok = torch.empty(P, dtype=torch.int32, device="cuda")
+    ent = torch.empty(P, dtype=torch.float32, device="cuda")
+    pm = torch.empty(P, dtype=torch.float32, device="cuda")
+    acc = torch.empty(P, dtype=torch.uint8, device="cuda")
+    cfg = B.make_sampler(P, V, 1.0, 0, 40.0, 0, seed)
+    ws = torch.empty(B.moe_w4a16_sampler_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+
+    def call(i, lg):
+        cfg.step = i
+        B.moe_w4a16_sample(cfg, lg, revealed, tok, ent, pm, acc, ws)
+
+    for i in range(warmup):
+        call(i, dev[i % 2])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e0.record()
+        for i in range(steps):
+            call(i, dev[i % 2])
+        e1.record()
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    # end to end: pinned host logits in, the four outputs back, every step
+    pinned = [torch.from_numpy(h).pin_memory() for h in host]
+    outs_h = [torch.empty(P, dtype=t.dtype, pin_memory=True) for t in (tok, ent, pm, acc)]
+    e2e_steps = max(3, min(50, steps))
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(e2e_steps):
+        dev[0].copy_(pinned[i % 2], non_blocking=True)
+        call(i, dev[0])
+        for o, d in zip(outs_h, (tok, ent, pm, acc)):
+            o.copy_(d, non_blocking=True)
+    t1.record()
+    torch.cuda.synchronize()
+    e2e_ms = t0.elapsed_time(t1) / e2e_steps
+    bytes_step = P * V * 4
+    peak, peak_src = measured_peak()
+    achieved = bytes_step / (ms * 1e-3) / 1e9
+    traffic = None
+    if os.path.exists(SAMPLER_PROFILE):
+        vals = dict(ln.split(":", 1) for ln in open(SAMPLER_PROFILE) if ":" in ln)
+        vals = {k.strip(): v.strip() for k, v in vals.items()}
+        if vals.get("kernel_source_sha256_16") == source_hash(SAMPLER_SRC):
+            try:
+                traffic = float(vals["traffic_bytes_per_launch_full_size"])
+            except (KeyError, ValueError):
+                traffic = None
+    res = {
+        "metric": SAMPLER_METRIC, "value": 1e3 / ms, "unit": "steps/s", "n_gpus": 1, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "sampler_p256_v262144", "positions": P, "vocab": V, "logits": "3 * N(0, 1) fp32",
+                   "rule": "entropy bound 40", "l2": "inputs larger than L2: 268 MB of logits per step vs 129 MB "
+                                                    "L2; two copies alternate"},
+        "roofline": {"kernel": "sample_pass_kernel + sample_final_kernel (the whole call: one streaming pass over "
+                               "the logits, then one CTA merging the partials and deciding the acceptance)",
+                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_src, "traffic": traffic, "algorithmic_bytes_per_launch": bytes_step},
+        "e2e": {"value": 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": bytes_step,
+                "d2h_bytes_per_step": P * (4 + 4 + 4 + 1), "steps": e2e_steps},
+        "gpu_launches": 2 * steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        nth = os.cpu_count() or 1
+        sample_p = 32
+        t = time.perf_counter()
+        oracle.sample(host[0][:sample_p], 1.0, seed, 0, nthreads=nth)
+        secs = time.perf_counter() - t
+        res["cpu_baseline"] = {"value": 1.0 / (secs * P / sample_p), "unit": "steps/s", "cores": nth,
+                               "kind": "oracle", "sample": f"{sample_p} of the {P} positions (fp64 entropy, "
+                                                           f"Gumbel keys of all {V} tokens), {nth} threads, "
+                                                           "scaled to a full step"}
+    return res
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.sampler:
+        print(json.dumps(run_sampler(args)), flush=True)
+        return
     if args.impl == "reference":
         # host-only: rank 0 times the oracle, the other ranks exit without work
         rank = int(os.environ.get("RANK", "0"))

@@ -189,6 +189,53 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_combine(const moe_w4a16_shape* shape, c
 MOE_W4A16_API moe_w4a16_status moe_w4a16_read_error(const void* workspace, size_t workspace_bytes, void* stream,
                                       moe_w4a16_status* device_status);
 
+/* ---- per-step sampler ------------------------------------------------------
+ * One denoising step's sampling over a canvas (model card
+ * "srswti/axe-diffusion-ksl-xe", "the kernels we built": the entropy once per
+ * step in a single streaming pass over the logits, one Gumbel-max kernel instead
+ * of softmax + multinomial; "lablup/mlxcel block-diffusion docs", "Samplers":
+ * the two acceptance rules).  Per position p, with t_v = logits[p][v] * inv_temperature:
+ *   entropy[p]  H = -sum_v q_v ln q_v of q = softmax(t)                    (fp32)
+ *   pmax[p]     max_v q_v                                                  (fp32)
+ *   token[p]    argmax_v (t_v + G_v), ties to the lower v; G_v = -ln(-ln U_v),
+ *               U_v = ((x & 0x7fffff) + 1/2) 2^-23, x = word v % 4 of Philox4x32-10
+ *               (Salmon et al., SC'11) at counter (v / 4, p, step, 0) under key
+ *               (seed & 0xffffffff, seed >> 32); the key is evaluated in fp32 with
+ *               one IEEE rounding per step (the natural log as range reduction plus
+ *               the atanh series to s^11, then fma(logit, inv_temperature, G)), so
+ *               the token is reproducible bit for bit off the GPU
+ *   accept[p]   rule 0 (entropy bound): among positions with revealed[p] == 0,
+ *               sorted by (entropy, p), sorted position i is accepted iff
+ *               fl(c_i - x_i) <= bound, c_i / x_i the fp32 running sum / maximum of
+ *               the sorted entropies (the mlx-vlm rule (cumsum - cummax) <= bound),
+ *               and the first one always;
+ *               rule 1 (confidence): revealed[p] == 0 and pmax[p] > bound; if no
+ *               such position, the unrevealed one with the largest pmax (ties to
+ *               the lower p).  Revealed positions are never accepted.
+ * Non-finite logits give unspecified (but in-bounds) results. */
+typedef struct {
+  int32_t positions;      /* P, 1 .. 1024 */
+  int32_t vocab;          /* V, a multiple of 4, 4 .. 2^30 */
+  float inv_temperature;  /* > 0 and finite */
+  int32_t rule;           /* 0 = entropy bound, 1 = confidence threshold */
+  float bound;            /* entropy bound (rule 0) or confidence threshold (rule 1), finite */
+  uint32_t step;          /* denoising step: third Philox counter word */
+  uint64_t seed;          /* Philox key */
+} moe_w4a16_sampler;
+
+/* Device workspace bytes moe_w4a16_sample needs (0 on an invalid config). */
+MOE_W4A16_API size_t moe_w4a16_sampler_workspace_bytes(const moe_w4a16_sampler* cfg);
+
+/* Runs the sampler on `stream` (two launches).  Device pointers:
+ *   logits    fp32 [P][V], 16-byte aligned        revealed  uint8 [P] (nonzero = already revealed)
+ *   token     int32 [P], entropy fp32 [P], pmax fp32 [P] (4-byte aligned), accept uint8 [P]
+ *   workspace moe_w4a16_sampler_workspace_bytes(cfg) bytes, 16-byte aligned (scratch, no state)
+ * ERR_SHAPE on an invalid config, ERR_NULL / ERR_ALIGN / ERR_WORKSPACE as elsewhere. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_sample(const moe_w4a16_sampler* cfg, const float* logits,
+                                                const uint8_t* revealed, int32_t* token, float* entropy,
+                                                float* pmax, uint8_t* accept, void* workspace,
+                                                size_t workspace_bytes, void* stream);
+
 /* ---- host-side weight helpers (no GPU needed) ---------------------------- */
 
 /* Canonical packing of uint4 codes (dg-w4a16-v1 style, model card

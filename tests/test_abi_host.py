@@ -206,3 +206,34 @@ def test_prepare_rejects_out_of_range_scale_and_zero():
     z[1, 2, 3] = np.float16(-0.5).view(np.uint16)
     with pytest.raises(B.MoeW4A16Error):
         B.moe_w4a16_prepare(sh, B.GATE_UP, w["gate_up_q"], w["gate_up_scale"], z)
+
+
+SAMPLER_VALID = dict(positions=8, vocab=4096, inv_temperature=1.0, rule=0, bound=1.0, step=0, seed=0)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(positions=0), dict(positions=1025), dict(vocab=0), dict(vocab=4098), dict(vocab=(1 << 30) + 4),
+    dict(inv_temperature=0.0), dict(inv_temperature=-1.0), dict(inv_temperature=float("inf")),
+    dict(inv_temperature=float("nan")), dict(rule=2), dict(bound=float("nan")), dict(bound=float("inf")),
+])
+def test_sampler_invalid_configs_rejected(bad):
+    d = dict(SAMPLER_VALID)
+    d.update(bad)
+    cfg = B.make_sampler(**d)
+    assert B.moe_w4a16_sampler_workspace_bytes(cfg) == 0
+    L = B.lib()
+    assert L.moe_w4a16_sample(ctypes.byref(cfg), 16, 16, 16, 16, 16, 16, 16, 1 << 30, None) == B.ERR_SHAPE
+
+
+def test_sampler_host_validation():
+    cfg = B.make_sampler(**SAMPLER_VALID)
+    need = B.moe_w4a16_sampler_workspace_bytes(cfg)
+    assert need == 8 * 1 * 32  # one 32-byte partial per position and vocabulary split of 32768
+    assert B.moe_w4a16_sampler_workspace_bytes(B.make_sampler(**dict(SAMPLER_VALID, vocab=262144))) == 8 * 8 * 32
+    L = B.lib()
+    assert L.moe_w4a16_sample(None, 16, 16, 16, 16, 16, 16, 16, need, None) == B.ERR_NULL
+    assert L.moe_w4a16_sample(ctypes.byref(cfg), None, 16, 16, 16, 16, 16, 16, need, None) == B.ERR_NULL
+    assert L.moe_w4a16_sample(ctypes.byref(cfg), 16, 16, 16, 16, 16, 16, None, need, None) == B.ERR_NULL
+    assert L.moe_w4a16_sample(ctypes.byref(cfg), 8, 16, 16, 16, 16, 16, 16, need, None) == B.ERR_ALIGN
+    assert L.moe_w4a16_sample(ctypes.byref(cfg), 16, 16, 18, 16, 16, 16, 16, need, None) == B.ERR_ALIGN
+    assert L.moe_w4a16_sample(ctypes.byref(cfg), 16, 16, 16, 16, 16, 16, 16, need - 1, None) == B.ERR_WORKSPACE

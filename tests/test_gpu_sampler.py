@@ -1,0 +1,122 @@
+"""The per-step sampler through the C ABI against the CPU oracle (sampler_oracle.c).
+
+Bars:
+  token     equal element for element (the Gumbel keys are defined in fp32 operation
+            by operation, so the argmax is the same integer on both sides);
+  entropy   |gpu - oracle| <= 2e-5 + 2e-5 |oracle| (fp32 streaming sums against fp64);
+  pmax      relative 2e-5;
+  accept    equal to the oracle's rule applied to the GPU's own fp32 entropy / pmax
+            (the rule is decided in fp32; the values themselves are checked above);
+  determinism  repeated calls bit-identical.
+Inputs: fp32 logits sigma * N(0, 1) (sigma 1 or 3) with a few peaked positions, as an
+LM head's logits over a 262,144-token vocabulary look at the scale the model card
+gives (268 MB of fp32 logits for a 256-token canvas).
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+NCPU = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from w4a16_moe_expert_router_gb300 import build as libbuild
+    libbuild.build()
+    from w4a16_moe_expert_router_gb300 import binding
+    return binding
+
+
+def _logits(P, V, sigma, seed):
+    rng = np.random.default_rng(seed)
+    lg = (rng.standard_normal((P, V), dtype=np.float32) * sigma).astype(np.float32)
+    for p in range(0, P, 5):  # peaked positions: low entropy, confident
+        lg[p, rng.integers(0, V)] += 12.0
+    return lg
+
+
+def _gpu_sample(B, lg, revealed, inv_temp, rule, bound, seed, step, repeats=1):
+    P, V = lg.shape
+    cfg = B.make_sampler(P, V, inv_temp, rule, bound, step, seed)
+    ws = torch.empty(B.moe_w4a16_sampler_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
+    d_lg = torch.from_numpy(lg).cuda()
+    d_rev = torch.from_numpy(revealed).cuda()
+    outs = []
+    for _ in range(repeats):
+        tok = torch.empty(P, dtype=torch.int32, device="cuda")
+        ent = torch.empty(P, dtype=torch.float32, device="cuda")
+        pm = torch.empty(P, dtype=torch.float32, device="cuda")
+        acc = torch.empty(P, dtype=torch.uint8, device="cuda")
+        B.moe_w4a16_sample(cfg, d_lg, d_rev, tok, ent, pm, acc, ws)
+        outs.append((tok, ent, pm, acc))
+    torch.cuda.synchronize()
+    return [tuple(t.cpu().numpy() for t in o) for o in outs]
+
+
+def _check(lg, revealed, inv_temp, rule, bound, seed, step, got):
+    tok, ent, pm, acc = got
+    o_tok, o_ent, o_pm = oracle.sample(lg, inv_temp, seed, step, nthreads=NCPU)
+    assert np.array_equal(tok, o_tok), np.nonzero(tok != o_tok)[0][:10]
+    assert np.all(np.abs(ent.astype(np.float64) - o_ent) <= 2e-5 + 2e-5 * np.abs(o_ent)), \
+        float(np.abs(ent - o_ent).max())
+    assert np.all(np.abs(pm.astype(np.float64) - o_pm) <= 2e-5 * o_pm), float(np.abs(pm / o_pm - 1).max())
+    want = (oracle.accept_entropy(ent, revealed, bound) if rule == 0
+            else oracle.accept_confidence(pm, revealed, bound))
+    assert np.array_equal(acc, want)
+
+
+@pytest.mark.parametrize("P,V,sigma,inv_temp,rule,bound", [
+    (8, 4096, 1.0, 1.0, 0, 5.0),
+    (3, 4100, 3.0, 0.7, 1, 0.5),          # one split, vocabulary not a multiple of the thread stride
+    (5, 70000, 1.0, 1.0, 0, 30.0),        # three splits, ragged last split
+    (1, 4, 2.0, 1.3, 0, 0.0),             # smallest vocabulary
+    (17, 65544, 3.0, 1.0, 1, 0.9),        # two full splits and 8 elements
+    (64, 32768, 1.0, 2.0, 0, 1.0),
+], ids=lambda v: str(v))
+def test_sampler_matches_oracle(B, P, V, sigma, inv_temp, rule, bound):
+    lg = _logits(P, V, sigma, seed=P * 1000 + V)
+    revealed = (np.arange(P) % 3 == 1).astype(np.uint8)
+    (got,) = _gpu_sample(B, lg, revealed, inv_temp, rule, bound, seed=0x1234_5678_9abc_def0 + P, step=V % 97)
+    _check(lg, revealed, inv_temp, rule, bound, 0x1234_5678_9abc_def0 + P, V % 97, got)
+
+
+def test_sampler_ties_and_dominant_logits(B):
+    """Equal logits (the noise alone decides) and one overwhelming logit per position."""
+    P, V = 6, 8192
+    lg = np.zeros((P, V), np.float32)
+    lg[3:, 100] = 60.0
+    revealed = np.zeros(P, np.uint8)
+    (got,) = _gpu_sample(B, lg, revealed, 1.0, 0, 2.0, seed=9, step=3)
+    _check(lg, revealed, 1.0, 0, 2.0, 9, 3, got)
+    assert np.all(got[0][3:] == 100)
+
+
+@pytest.mark.parametrize("rule,bound", [(0, 40.0), (1, 0.5)])
+def test_sampler_full_canvas_step(B, rule, bound):
+    """256 positions x 262,144 vocabulary (268 MB of fp32 logits), every position checked;
+    three repeated calls bit-identical."""
+    P, V = 256, 262144
+    lg = _logits(P, V, 3.0, seed=rule)
+    revealed = np.zeros(P, np.uint8)
+    revealed[::4] = 1
+    outs = _gpu_sample(B, lg, revealed, 1.0, rule, bound, seed=77, step=5, repeats=3)
+    for o in outs[1:]:
+        for a, b in zip(o, outs[0]):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+    _check(lg, revealed, 1.0, rule, bound, 77, 5, outs[0])
+    assert outs[0][3].sum() >= 1
+
+
+def test_sampler_all_revealed_accepts_nothing(B):
+    P, V = 4, 4096
+    lg = _logits(P, V, 1.0, 5)
+    (got,) = _gpu_sample(B, lg, np.ones(P, np.uint8), 1.0, 0, 10.0, seed=1, step=0)
+    assert got[3].sum() == 0

@@ -26,7 +26,7 @@ EXPORTED = ("moe_w4a16_workspace_bytes", "moe_w4a16_workspace_init", "moe_w4a16_
             "moe_w4a16_experts",
             "moe_w4a16_gate_up", "moe_w4a16_down", "moe_w4a16_combine", "moe_w4a16_read_error", "moe_w4a16_pack", "moe_w4a16_unpack", "moe_w4a16_prepared_bytes",
             "moe_w4a16_prepare", "moe_w4a16_unprepare", "moe_w4a16_status_string", "moe_w4a16_forward_noalloc",
-            "moe_w4a16_selftest_wait_timeout")
+            "moe_w4a16_selftest_wait_timeout", "moe_w4a16_sampler_workspace_bytes", "moe_w4a16_sample")
 
 NOALLOC_SCRATCH_BYTES = 40 << 20  # MOE_W4A16_NOALLOC_SCRATCH_BYTES
 
@@ -40,6 +40,12 @@ class MoeW4A16Error(RuntimeError):
 class Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("tokens", "hidden", "inter", "experts", "top_k", "group_gate_up",
                                               "group_down", "activation", "reduction")]
+
+
+class Sampler(ctypes.Structure):
+    _fields_ = [("positions", ctypes.c_int32), ("vocab", ctypes.c_int32), ("inv_temperature", ctypes.c_float),
+                ("rule", ctypes.c_int32), ("bound", ctypes.c_float), ("step", ctypes.c_uint32),
+                ("seed", ctypes.c_uint64)]
 
 
 class Weights(ctypes.Structure):
@@ -87,6 +93,10 @@ def lib() -> ctypes.CDLL:
             L.moe_w4a16_forward_noalloc.restype = st
             L.moe_w4a16_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint64, vp]
             L.moe_w4a16_selftest_wait_timeout.restype = st
+            L.moe_w4a16_sampler_workspace_bytes.argtypes = [P(Sampler)]
+            L.moe_w4a16_sampler_workspace_bytes.restype = sz
+            L.moe_w4a16_sample.argtypes = [P(Sampler), vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.moe_w4a16_sample.restype = st
             L.moe_w4a16_read_error.argtypes = [vp, sz, vp, P(ctypes.c_int)]
             L.moe_w4a16_read_error.restype = st
             L.moe_w4a16_pack.argtypes = [vp, i64, i64, vp]
@@ -222,6 +232,20 @@ def moe_w4a16_combine(shape: Shape, routing: RoutingBuffers, norm_gamma, norm_ep
     _check(lib().moe_w4a16_combine(ctypes.byref(shape), ctypes.byref(r), _dptr(norm_gamma), float(norm_eps),
                                    _dptr(out), _dptr(workspace), _nbytes(workspace), _stream(stream)),
            "moe_w4a16_combine")
+
+
+def make_sampler(positions, vocab, inv_temperature=1.0, rule=0, bound=0.0, step=0, seed=0) -> Sampler:
+    return Sampler(positions, vocab, inv_temperature, rule, bound, step, seed)
+
+
+def moe_w4a16_sampler_workspace_bytes(cfg: Sampler) -> int:
+    return int(lib().moe_w4a16_sampler_workspace_bytes(ctypes.byref(cfg)))
+
+
+def moe_w4a16_sample(cfg: Sampler, logits, revealed, token, entropy, pmax, accept, workspace, stream=None) -> None:
+    _check(lib().moe_w4a16_sample(ctypes.byref(cfg), _dptr(logits), _dptr(revealed), _dptr(token), _dptr(entropy),
+                                  _dptr(pmax), _dptr(accept), _dptr(workspace), _nbytes(workspace), _stream(stream)),
+           "moe_w4a16_sample")
 
 
 def moe_w4a16_read_error(workspace, stream=None) -> int:

@@ -103,6 +103,37 @@ moe_w4a16_status moe_w4a16_selftest_wait_timeout(void* workspace, size_t workspa
   return cuda_status(moe::launch_wait_selftest(&hdr->error, &hdr->never_set, limit_ns, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+bool sampler_ok(const moe_w4a16_sampler* c) {
+  return c->positions >= 1 && c->positions <= moe::kSamplerMaxPositions && c->vocab >= 4 && c->vocab % 4 == 0 &&
+         c->vocab <= (1 << 30) && c->inv_temperature > 0.f && c->inv_temperature <= 3.4e38f &&
+         (c->rule == 0 || c->rule == 1) && c->bound >= -3.4e38f && c->bound <= 3.4e38f;
+}
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+}  // namespace
+
+size_t moe_w4a16_sampler_workspace_bytes(const moe_w4a16_sampler* cfg) {
+  if (!cfg || !sampler_ok(cfg)) return 0;
+  return moe::sampler_ws_bytes(cfg->positions, cfg->vocab);
+}
+
+moe_w4a16_status moe_w4a16_sample(const moe_w4a16_sampler* cfg, const float* logits, const uint8_t* revealed,
+                                  int32_t* token, float* entropy, float* pmax, uint8_t* accept, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (!cfg) return MOE_W4A16_ERR_NULL;
+  if (!sampler_ok(cfg)) return MOE_W4A16_ERR_SHAPE;
+  if (!logits || !revealed || !token || !entropy || !pmax || !accept || !workspace) return MOE_W4A16_ERR_NULL;
+  if (!aligned16(logits) || !aligned16(workspace) || !aligned4(token) || !aligned4(entropy) || !aligned4(pmax))
+    return MOE_W4A16_ERR_ALIGN;
+  if (workspace_bytes < moe::sampler_ws_bytes(cfg->positions, cfg->vocab)) return MOE_W4A16_ERR_WORKSPACE;
+  moe_w4a16_status st;
+  const DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != MOE_W4A16_OK) return st;
+  return cuda_status(moe::launch_sample(cfg->positions, cfg->vocab, cfg->inv_temperature, cfg->seed, cfg->step,
+                                        cfg->rule, cfg->bound, logits, revealed, token, entropy, pmax, accept,
+                                        workspace, static_cast<cudaStream_t>(stream)));
+}
+
 moe_w4a16_status moe_w4a16_route(const moe_w4a16_shape* shape, const float* logits, const moe_w4a16_routing* out,
                                  void* workspace, size_t workspace_bytes, void* stream) {
   Dims s;

@@ -106,6 +106,19 @@ cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, cons
 cudaError_t launch_combine(const Dims& s, const float* topk_w, const float* y, const float* gamma, float eps,
                            uint16_t* out, cudaStream_t st);
 
+// Per-step sampler (sampler.cu): one streaming pass over the logits (grid of
+// vocabulary splits x positions) writing 32-byte partials to the workspace, then
+// one CTA that merges them and applies the acceptance rule.
+constexpr int kSamplerChunk = 32768;        // vocabulary elements per CTA of the pass
+constexpr int kSamplerMaxPositions = 1024;  // one thread per position in the final CTA
+int sampler_splits(int64_t vocab);
+inline size_t sampler_ws_bytes(int positions, int64_t vocab) {
+  return size_t(positions) * size_t(sampler_splits(vocab)) * 32;
+}
+cudaError_t launch_sample(int P, int64_t V, float inv_temp, uint64_t seed, uint32_t step, int rule, float bound,
+                          const float* logits, const uint8_t* revealed, int32_t* token, float* entropy, float* pmax,
+                          uint8_t* accept, void* workspace, cudaStream_t st);
+
 // Self-test of the expert launch's bounded waits: waits that cannot complete (an
 // mbarrier phase, then the counter *flag, which must stay 0) give up after limit_ns
 // each and record MOE_W4A16_ERR_TIMEOUT in *err.
