@@ -41,7 +41,7 @@ def build(force: bool = False) -> str:
 
 class _Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("tokens", "hidden", "inter", "experts", "top_k",
-                                              "group_gate_up", "group_down", "activation")]
+                                              "group_gate_up", "group_down", "activation", "format")]
 
 
 class _Weights(ctypes.Structure):
@@ -65,6 +65,8 @@ def lib():
             L.oracle_code.argtypes = [vp, i64]
             L.oracle_dequant.argtypes = [ctypes.c_int, ctypes.c_uint16, ctypes.c_uint16]
             L.oracle_dequant.restype = dbl
+            L.oracle_dequant_format.argtypes = [ctypes.c_int, ctypes.c_uint16, ctypes.c_uint16, ctypes.c_int]
+            L.oracle_dequant_format.restype = dbl
             L.oracle_gelu.argtypes = [dbl, ctypes.c_int]
             L.oracle_gelu.restype = dbl
             L.oracle_rmsnorm.argtypes = [i64, vp, vp, dbl, vp]
@@ -110,6 +112,11 @@ def dequant(q: int, zero_bits: int, scale_bits: int) -> float:
     return lib().oracle_dequant(int(q), int(zero_bits), int(scale_bits))
 
 
+def dequant_format(q: int, second_bits: int, scale_bits: int, fmt: int) -> float:
+    """One weight of format 0 (asymmetric zero-point), 1 (affine bias) or 2 (symmetric)."""
+    return lib().oracle_dequant_format(int(q), int(second_bits), int(scale_bits), int(fmt))
+
+
 def gelu(a: float, act: int = 0) -> float:
     return lib().oracle_gelu(float(a), int(act))
 
@@ -146,8 +153,8 @@ def rmsnorm(u: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     return out
 
 
-def _shape(T, d, f, E, k, g1, g2, act):
-    return _Shape(T, d, f, E, k, g1, g2, act)
+def _shape(T, d, f, E, k, g1, g2, act, fmt=0):
+    return _Shape(T, d, f, E, k, g1, g2, act, fmt)
 
 
 def _weights(w: dict):
@@ -162,7 +169,7 @@ def _weights(w: dict):
 def forward(x_bits: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, weights: dict, *,
             group_gate_up: int, group_down: int, activation: int = 0, gamma: np.ndarray | None = None,
             eps: float = 1e-6, token_sel: np.ndarray | None = None, nthreads: int = 1,
-            round_fp16: bool = False) -> np.ndarray:
+            round_fp16: bool = False, fmt: int = 0) -> np.ndarray:
     """The layer (sparse form).  Returns fp64 [T][d]; unselected tokens stay NaN.
 
     x_bits: fp16 bit patterns [T][d] (uint16); weights: canonical arrays
@@ -176,7 +183,7 @@ def forward(x_bits: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, weight
     k = idx.shape[1]
     E, two_f, _ = weights["gate_up_q"].shape
     f = two_f // 2
-    sh = _shape(T, d, f, E, k, group_gate_up, group_down, activation)
+    sh = _shape(T, d, f, E, k, group_gate_up, group_down, activation, fmt)
     cw, keep = _weights(weights)
     g = None if gamma is None else _c(gamma, np.float32)
     sel = None if token_sel is None else _c(token_sel, np.uint8)
@@ -190,7 +197,7 @@ def forward(x_bits: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, weight
 
 
 def forward_dense(x_bits: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, weights: dict, *,
-                  group_gate_up: int, group_down: int, activation: int = 0) -> np.ndarray:
+                  group_gate_up: int, group_down: int, activation: int = 0, fmt: int = 0) -> np.ndarray:
     """The layer (dense form: every expert on every token, gated by G[t][e])."""
     x = _c(x_bits, np.uint16)
     idx = _c(topk_idx, np.int32)
@@ -198,7 +205,7 @@ def forward_dense(x_bits: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, 
     T, d = x.shape
     k = idx.shape[1]
     E, two_f, _ = weights["gate_up_q"].shape
-    sh = _shape(T, d, two_f // 2, E, k, group_gate_up, group_down, activation)
+    sh = _shape(T, d, two_f // 2, E, k, group_gate_up, group_down, activation, fmt)
     cw, keep = _weights(weights)
     out = np.zeros((T, d), np.float64)
     st = lib().oracle_moe_forward_dense(ctypes.byref(sh), _ptr(x), _ptr(idx), _ptr(wt), ctypes.byref(cw), _ptr(out))

@@ -172,15 +172,28 @@ double oracle_dequant(int q, uint16_t zero_bits, uint16_t scale_bits) {
   return ((double)q - oracle_half_to_double(zero_bits)) * oracle_half_to_double(scale_bits);
 }
 
+/* The three checkpoint formats, each with one fp16 scale s and one fp16 second
+ * value per group ([TF] "Summary": symmetric GPTQ 4/128 and MLX affine 4/64 next
+ * to the model card's asymmetric uint4):
+ *   format 0  asymmetric zero-point   w = (q - z) s      (second value z)
+ *   format 1  affine bias (MLX)       w = q s + b        (second value b)
+ *   format 2  symmetric (GPTQ)        w = (q - 8) s      (second value unused) */
+double oracle_dequant_format(int q, uint16_t second_bits, uint16_t scale_bits, int format) {
+  const double s = oracle_half_to_double(scale_bits);
+  if (format == 1) return (double)q * s + oracle_half_to_double(second_bits);
+  if (format == 2) return ((double)q - 8.0) * s;
+  return ((double)q - oracle_half_to_double(second_bits)) * s;
+}
+
 /* Dense fp64 copy of one quantised matrix W [rows][K]:
  *   packed [rows][K/2] bytes, scale/zero [rows][K/g] fp16 bits. */
 static void dequant_matrix(int64_t rows, int64_t K, int g, const uint8_t* packed, const uint16_t* scale,
-                           const uint16_t* zero, int round_fp16, double* W) {
+                           const uint16_t* zero, int format, int round_fp16, double* W) {
   int64_t ng = K / g;
   for (int64_t n = 0; n < rows; ++n) {
     for (int64_t kk = 0; kk < K; ++kk) {
       int q = oracle_code(packed + n * (K / 2), kk);
-      double w = oracle_dequant(q, zero[n * ng + kk / g], scale[n * ng + kk / g]);
+      double w = oracle_dequant_format(q, zero[n * ng + kk / g], scale[n * ng + kk / g], format);
       if (round_fp16) w = oracle_half_to_double(oracle_double_to_half(w));
       W[n * K + kk] = w;
     }
@@ -202,6 +215,7 @@ double oracle_gelu(double a, int act) {
 
 typedef struct {
   int32_t tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation;
+  int32_t format; /* 0 asymmetric zero-point, 1 affine bias, 2 symmetric (see oracle_dequant_format) */
 } oracle_shape;
 
 typedef struct {
@@ -220,6 +234,7 @@ static int shape_ok(const oracle_shape* s) {
   if (s->group_gate_up < 2 || s->group_down < 2) return 0;
   if (s->hidden % s->group_gate_up || s->inter % s->group_down) return 0;
   if (s->group_gate_up % 2 || s->group_down % 2) return 0;
+  if (s->format < 0 || s->format > 2) return 0;
   return s->activation == 0 || s->activation == 1;
 }
 
@@ -276,10 +291,10 @@ static void* expert_worker(void* arg) {
     int64_t ng1 = d / s->group_gate_up, ng2 = f / s->group_down;
     dequant_matrix(2 * f, d, s->group_gate_up, j->w->gate_up_q + (int64_t)e * 2 * f * (d / 2),
                    j->w->gate_up_scale + (int64_t)e * 2 * f * ng1, j->w->gate_up_zero + (int64_t)e * 2 * f * ng1,
-                   j->round_fp16, Wgu);
+                   s->format, j->round_fp16, Wgu);
     dequant_matrix(d, f, s->group_down, j->w->down_q + (int64_t)e * d * (f / 2),
                    j->w->down_scale + (int64_t)e * d * ng2, j->w->down_zero + (int64_t)e * d * ng2,
-                   j->round_fp16, Wd);
+                   s->format, j->round_fp16, Wd);
     for (int64_t p = 0; p < T * k; ++p) {
       if (j->topk_idx[p] != e) continue;
       int64_t t = p / k;
@@ -382,9 +397,9 @@ int oracle_moe_forward_dense(const oracle_shape* s, const uint16_t* x, const int
   for (int64_t i = 0; i < T * d; ++i) out[i] = 0.0;
   for (int64_t e = 0; e < E; ++e) {
     dequant_matrix(2 * f, d, s->group_gate_up, w->gate_up_q + e * 2 * f * (d / 2), w->gate_up_scale + e * 2 * f * ng1,
-                   w->gate_up_zero + e * 2 * f * ng1, 0, Wgu);
+                   w->gate_up_zero + e * 2 * f * ng1, s->format, 0, Wgu);
     dequant_matrix(d, f, s->group_down, w->down_q + e * d * (f / 2), w->down_scale + e * d * ng2,
-                   w->down_zero + e * d * ng2, 0, Wd);
+                   w->down_zero + e * d * ng2, s->format, 0, Wd);
     for (int64_t t = 0; t < T; ++t) {
       for (int64_t i = 0; i < d; ++i) xd[i] = oracle_half_to_double(x[t * d + i]);
       expert_ffn(s, Wgu, Wd, xd, 0, a, h, y);

@@ -314,3 +314,32 @@ def test_fp16_diagnostic_mode_stays_within_rounding():
     rounded = oracle.forward(x, idx, w, wts, group_gate_up=64, group_down=64, round_fp16=True)
     rel = np.linalg.norm(rounded - exact) / np.linalg.norm(exact)
     assert 0 < rel < 2e-3
+
+
+# ---------------------------------------------------------------- formats
+# "ashhart/TensorFold pull 802", "Summary": symmetric GPTQ 4/128 and MLX affine 4/64
+# checkpoints next to the model card's asymmetric uint4 (format 0).
+
+def test_format_dequant_values():
+    s, z, b = 0x211F, 0x47C0, 0xAC00  # fp16 0.0100021..., 7.75, -0.0625
+    sv, zv, bv = (float(np.array([v], np.uint16).view(np.float16)[0]) for v in (s, z, b))
+    for q in (0, 7, 8, 15):
+        assert oracle.dequant_format(q, z, s, 0) == (q - zv) * sv
+        assert oracle.dequant_format(q, b, s, 1) == q * sv + bv
+        assert oracle.dequant_format(q, z, s, 2) == (q - 8) * sv
+
+
+def test_format_identities_through_the_layer():
+    """Affine with b = 0 is asymmetric with z = 0, and symmetric is asymmetric with
+    z = 8, bit for bit through the whole fp64 layer; a swapped or miswired format fails."""
+    wl = synth.Workload("fmt", 9, 256, 64, 4, 2, 64, 32)
+    x, lg = synth.make_x(wl, 3), synth.make_logits(wl, 3)
+    w = synth.make_weights(wl, 3)
+    idx, tw = oracle.route(lg, wl.top_k)
+    zero = {k: (np.zeros_like(v) if k.endswith("zero") else v) for k, v in w.items()}
+    eight = {k: (np.full_like(v, 0x4800) if k.endswith("zero") else v) for k, v in w.items()}
+    run = lambda ww, fmt: oracle.forward(x, idx, tw, ww, group_gate_up=64, group_down=32, fmt=fmt)
+    assert np.array_equal(run(zero, 1), run(zero, 0))
+    assert np.array_equal(run(w, 2), run(eight, 0))
+    assert not np.array_equal(run(w, 2), run(w, 0))
+    assert not np.array_equal(run(w, 1), run(w, 0))

@@ -46,6 +46,7 @@ class Workload:
     rmsnorm: bool = False      # fp32 RMSNorm after every layer (gamma ~ N(1, 0.1))
     activation: int = 0        # 0 = GELU tanh form, 1 = GELU erf form
     reduction: int = 0         # 0 = each weight dequantised, 1 = group-factorised expert GEMMs
+    format: int = 0            # 0 = asymmetric zero-point, 1 = affine bias (MLX), 2 = symmetric (GPTQ)
 
     def weight_bytes_per_expert(self) -> int:
         """Packed nibbles plus fp16 scale and zero of both projections."""
@@ -95,14 +96,27 @@ def make_weights(w: Workload, seed: int = 0, layer: int = 0) -> dict:
     down_q [E][d][f/2] u8, down_scale/zero [E][d][f/g2] fp16 bits.
     """
     E, d, f, g1, g2 = w.experts, w.hidden, w.inter, w.group_gate_up, w.group_down
+    gus = _half_bits(_rng(seed, layer, _GUS).uniform(0.005, 0.02, (E, 2 * f, d // g1)))
+    ds = _half_bits(_rng(seed, layer, _DS).uniform(0.005, 0.02, (E, d, f // g2)))
     return {
         "gate_up_q": _rng(seed, layer, _GUQ).integers(0, 256, (E, 2 * f, d // 2), dtype=np.uint8),
-        "gate_up_scale": _half_bits(_rng(seed, layer, _GUS).uniform(0.005, 0.02, (E, 2 * f, d // g1))),
-        "gate_up_zero": _half_bits(_rng(seed, layer, _GUZ).uniform(6.0, 9.0, (E, 2 * f, d // g1))),
+        "gate_up_scale": gus,
+        "gate_up_zero": _second(w, _rng(seed, layer, _GUZ).uniform(6.0, 9.0, (E, 2 * f, d // g1)), gus),
         "down_q": _rng(seed, layer, _DQ).integers(0, 256, (E, d, f // 2), dtype=np.uint8),
-        "down_scale": _half_bits(_rng(seed, layer, _DS).uniform(0.005, 0.02, (E, d, f // g2))),
-        "down_zero": _half_bits(_rng(seed, layer, _DZ).uniform(6.0, 9.0, (E, d, f // g2))),
+        "down_scale": ds,
+        "down_zero": _second(w, _rng(seed, layer, _DZ).uniform(6.0, 9.0, (E, d, f // g2)), ds),
     }
+
+
+def _second(w: Workload, z: np.ndarray, scale_bits: np.ndarray) -> np.ndarray:
+    """The per-group value stored beside the scale: the zero-point z (format 0), the
+    affine bias b = fp16(-z * s) of the same dequantised range (format 1), or 8 (format 2,
+    where it is not read)."""
+    if w.format == 1:
+        return _half_bits(-z * scale_bits.view(np.float16).astype(np.float64))
+    if w.format == 2:
+        return np.full(z.shape, 0x4800, np.uint16)
+    return _half_bits(z)
 
 
 def make_gamma(w: Workload, seed: int = 0, layer: int = 0) -> np.ndarray:
