@@ -88,9 +88,16 @@ typedef enum {
  *                     term -s z sum(x) added, group after group.  More accurate (no weight is
  *                     rounded to fp16); work items of at most 16 tokens, so slower than 0 when
  *                     experts get more than ~8 tokens each
+ *   format        weight format, one fp16 scale s and one fp16 second value per group
+ *                 ("ashhart/TensorFold pull 802", "Summary": symmetric GPTQ 4/128 and MLX affine
+ *                 4/64 checkpoints beside the model card's asymmetric uint4):
+ *                 0 = asymmetric zero-point, w = (q - z) s, 0 <= z <= 16 (dg-w4a16-v1);
+ *                 1 = affine bias (MLX), w = q s + b, |b| <= 1024 (the second value is b);
+ *                 2 = symmetric (GPTQ), w = (q - 8) s (no second value: moe_w4a16_prepare
+ *                     writes 8 and accepts zero == NULL)
  * T*k must not exceed 2^22. */
 typedef struct {
-  int32_t tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation, reduction;
+  int32_t tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation, reduction, format;
 } moe_w4a16_shape;
 
 /* Expert weights of one layer, in the prepared layout written by
@@ -257,8 +264,11 @@ MOE_W4A16_API size_t moe_w4a16_prepared_bytes(const moe_w4a16_shape* shape, int3
  *           MOE_W4A16_DOWN:    rows R = d, K = f, g = g2
  *   q       canonical packed codes [E][R][K/2]
  *   scale   fp16 bits [E][R][K/g]
- *   zero    fp16 bits [E][R][K/g]
+ *   zero    fp16 bits [E][R][K/g]: the zero-point (format 0) or the bias (format 1);
+ *           ignored and may be NULL for format 2 (the layout then holds 8)
  *   out     moe_w4a16_prepared_bytes(shape, which) bytes
+ * ERR_VALUE if |scale| > 32 or not finite, if a zero-point is outside [0, 16]
+ * (format 0) or a bias outside [-1024, 1024] (format 1).
  * The prepared layout is private to this library version: per block of 128 GEMM
  * rows, a stream of 128-column stages (the last of 64 columns when K is an odd
  * multiple of 64), each split into eight strips of 16 rows, one per compute warp;

@@ -57,7 +57,7 @@ def _shape(**kw):
 @pytest.mark.parametrize("bad", [
     dict(hidden=192), dict(hidden=64), dict(inter=96), dict(experts=0), dict(experts=257), dict(top_k=0),
     dict(top_k=9), dict(experts=4, top_k=5), dict(group_gate_up=48), dict(group_gate_up=16),
-    dict(group_down=128, inter=192), dict(activation=2), dict(reduction=2), dict(reduction=-1), dict(tokens=-1), dict(tokens=1 << 20, top_k=8),
+    dict(group_down=128, inter=192), dict(activation=2), dict(reduction=2), dict(reduction=-1), dict(format=3), dict(format=-1), dict(tokens=-1), dict(tokens=1 << 20, top_k=8),
 ])
 def test_invalid_shapes_rejected(bad):
     sh = _shape(**bad)
@@ -237,3 +237,31 @@ def test_sampler_host_validation():
     assert L.moe_w4a16_sample(ctypes.byref(cfg), 8, 16, 16, 16, 16, 16, 16, need, None) == B.ERR_ALIGN
     assert L.moe_w4a16_sample(ctypes.byref(cfg), 16, 16, 18, 16, 16, 16, 16, need, None) == B.ERR_ALIGN
     assert L.moe_w4a16_sample(ctypes.byref(cfg), 16, 16, 16, 16, 16, 16, 16, need - 1, None) == B.ERR_WORKSPACE
+
+
+def test_prepare_per_format():
+    """Format 1 keeps the bias in the zero-point slot and accepts negative values;
+    format 2 needs no zero array and stores 8 there; out-of-range values are refused."""
+    import dataclasses
+    base = synth.WORKLOADS["tiny"]
+    aff = dataclasses.replace(base, format=1)
+    w = synth.make_weights(aff)
+    assert (w["gate_up_zero"].view(np.float16) < 0).all()
+    sh = runtime.shape_of(aff)
+    prep = B.moe_w4a16_prepare(sh, B.GATE_UP, w["gate_up_q"], w["gate_up_scale"], w["gate_up_zero"])
+    with pytest.raises(B.MoeW4A16Error):  # a bias is not a valid zero-point
+        B.moe_w4a16_prepare(runtime.shape_of(base), B.GATE_UP, w["gate_up_q"], w["gate_up_scale"], w["gate_up_zero"])
+    b = w["gate_up_zero"].copy()
+    b[0, 0, 0] = np.float16(2000.0).view(np.uint16)
+    with pytest.raises(B.MoeW4A16Error) as e:
+        B.moe_w4a16_prepare(sh, B.GATE_UP, w["gate_up_q"], w["gate_up_scale"], b)
+    assert e.value.status == B.ERR_VALUE
+    sym = dataclasses.replace(base, format=2)
+    ws = synth.make_weights(sym)
+    sh2 = runtime.shape_of(sym)
+    p_none = B.moe_w4a16_prepare(sh2, B.DOWN, ws["down_q"], ws["down_scale"], None)
+    p_any = B.moe_w4a16_prepare(sh2, B.DOWN, ws["down_q"], ws["down_scale"], np.zeros_like(ws["down_zero"]))
+    p_eight = B.moe_w4a16_prepare(runtime.shape_of(base), B.DOWN, ws["down_q"], ws["down_scale"],
+                                  np.full_like(ws["down_zero"], 0x4800))
+    assert np.array_equal(p_none, p_any) and np.array_equal(p_none, p_eight)
+    assert prep.nbytes == B.moe_w4a16_prepared_bytes(sh, B.GATE_UP)

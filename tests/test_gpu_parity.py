@@ -92,7 +92,7 @@ def _full_case(rt, wl, seed=0, tokens=None, sel=None):
     routing, (out,) = _gpu_layer(rt, wl, x, lg, w)
     idx, tw = _check_routing(lg, wl.top_k, wl.experts, routing)
     ref = oracle.forward(x, idx, tw, w, group_gate_up=wl.group_gate_up, group_down=wl.group_down,
-                         activation=wl.activation, token_sel=sel, nthreads=NCPU)
+                         activation=wl.activation, token_sel=sel, nthreads=NCPU, fmt=wl.format)
     rows = None if sel is None else np.nonzero(sel)[0]
     return _check_out(out, ref, rows)
 
@@ -139,6 +139,20 @@ SHAPES = [
 def test_group_factorised_shape_variants(rt, wl):
     """The group-factorised order (reduction = 1) on the same shapes, held to the same bars."""
     _full_case(rt, wl, seed=5)
+
+
+@pytest.mark.parametrize("fmt", [1, 2], ids=["affine", "symmetric"])
+@pytest.mark.parametrize("reduction", [0, 1])
+@pytest.mark.parametrize("wl", [SHAPES[0], SHAPES[1], SHAPES[3], SHAPES[5]], ids=lambda w: w.name)
+def test_weight_formats(rt, wl, reduction, fmt):
+    """Affine-bias (MLX, w = q s + b) and symmetric (GPTQ, w = (q - 8) s) weights in
+    both reduction orders, held to the same bars against the oracle of that format."""
+    _full_case(rt, dataclasses.replace(wl, format=fmt, reduction=reduction), seed=6)
+
+
+@pytest.mark.parametrize("fmt", [1, 2], ids=["affine", "symmetric"])
+def test_weight_formats_canvas64_full_size(rt, fmt):
+    _full_case(rt, dataclasses.replace(synth.WORKLOADS["canvas64"], format=fmt))
 
 
 def test_group_factorised_canvas256_full_size(rt):

@@ -39,7 +39,7 @@ class MoeW4A16Error(RuntimeError):
 
 class Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("tokens", "hidden", "inter", "experts", "top_k", "group_gate_up",
-                                              "group_down", "activation", "reduction")]
+                                              "group_down", "activation", "reduction", "format")]
 
 
 class Sampler(ctypes.Structure):
@@ -118,8 +118,8 @@ def lib() -> ctypes.CDLL:
 # ----------------------------------------------------------------- marshalling
 
 def make_shape(tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation=0,
-               reduction=0) -> Shape:
-    return Shape(tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation, reduction)
+               reduction=0, format=0) -> Shape:
+    return Shape(tokens, hidden, inter, experts, top_k, group_gate_up, group_down, activation, reduction, format)
 
 
 def _dptr(t) -> int | None:
@@ -282,18 +282,19 @@ def moe_w4a16_prepared_bytes(shape: Shape, which: int) -> int:
     return int(lib().moe_w4a16_prepared_bytes(ctypes.byref(shape), int(which)))
 
 
-def moe_w4a16_prepare(shape: Shape, which: int, q: np.ndarray, scale: np.ndarray, zero: np.ndarray) -> np.ndarray:
+def moe_w4a16_prepare(shape: Shape, which: int, q: np.ndarray, scale: np.ndarray, zero) -> np.ndarray:
+    """zero: the zero-points (format 0) or biases (format 1); None allowed for format 2."""
     q = np.ascontiguousarray(q, dtype=np.uint8)
     s = np.ascontiguousarray(scale, dtype=np.uint16)
-    z = np.ascontiguousarray(zero, dtype=np.uint16)
+    z = None if zero is None else np.ascontiguousarray(zero, dtype=np.uint16)
     n = moe_w4a16_prepared_bytes(shape, which)
     if n == 0:
         raise MoeW4A16Error(ERR_SHAPE, "moe_w4a16_prepare")
-    if q.nbytes + s.nbytes + z.nbytes != n:
+    if q.nbytes + 2 * s.nbytes != n or (z is not None and z.nbytes != s.nbytes):
         raise MoeW4A16Error(ERR_SHAPE, "moe_w4a16_prepare: array sizes do not match the shape")
     out = np.empty(n, np.uint8)
-    _check(lib().moe_w4a16_prepare(ctypes.byref(shape), int(which), _hptr(q), _hptr(s), _hptr(z), _hptr(out)),
-           "moe_w4a16_prepare")
+    _check(lib().moe_w4a16_prepare(ctypes.byref(shape), int(which), _hptr(q), _hptr(s),
+                                   None if z is None else _hptr(z), _hptr(out)), "moe_w4a16_prepare")
     return out
 
 

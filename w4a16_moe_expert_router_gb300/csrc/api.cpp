@@ -21,7 +21,7 @@ bool pow2_group(int g) { return g == 32 || g == 64 || g == 128; }
 moe_w4a16_status check_shape(const moe_w4a16_shape* sh, Dims* out) {
   if (!sh) return MOE_W4A16_ERR_NULL;
   const Dims s{sh->tokens, sh->hidden, sh->inter, sh->experts, sh->top_k, sh->group_gate_up, sh->group_down,
-               sh->activation, sh->reduction};
+               sh->activation, sh->reduction, sh->format};
   if (s.T < 0) return MOE_W4A16_ERR_SHAPE;
   if (s.d < 128 || s.d % 128 != 0 || s.d > 8192) return MOE_W4A16_ERR_SHAPE;
   if (s.f < 64 || s.f % 64 != 0 || s.f > 16384) return MOE_W4A16_ERR_SHAPE;
@@ -31,6 +31,7 @@ moe_w4a16_status check_shape(const moe_w4a16_shape* sh, Dims* out) {
   if (!pow2_group(s.g2) || s.f % s.g2 != 0) return MOE_W4A16_ERR_SHAPE;
   if (s.act != 0 && s.act != 1) return MOE_W4A16_ERR_SHAPE;
   if (s.red != 0 && s.red != 1) return MOE_W4A16_ERR_SHAPE;
+  if (s.fmt < 0 || s.fmt > 2) return MOE_W4A16_ERR_SHAPE;
   if (s.pairs() > moe::kMaxPairs) return MOE_W4A16_ERR_SHAPE;
   if (out) *out = s;
   return MOE_W4A16_OK;

@@ -193,6 +193,22 @@ __device__ __forceinline__ DqRows dq_rows(uint32_t vx, uint32_t vy) {
   return k;
 }
 
+// The same constants for the affine format (w = q s + b, the second value of the
+// group is the bias b): the offset is the bare 1024 / 64, so the subtract gives q
+// exactly, and the fused multiply-add forms fp16(q s + b) with one rounding.
+__device__ __forceinline__ DqRows dq_rows_affine(uint32_t vx, uint32_t vy) {
+  const uint32_t bb = __byte_perm(vx, vy, 0x7632), ss = __byte_perm(vx, vy, 0x5410);
+  const __half2 b = bits_h2(bb), s = bits_h2(ss);
+  DqRows k;
+  k.zb_lo = bits_h2(0x64006400u);
+  k.s_lo = __low2half2(s);
+  k.c_lo = __low2half2(b);
+  k.zb_hi = bits_h2(0x54005400u);
+  k.s_hi = __high2half2(s);
+  k.c_hi = __high2half2(b);
+  return k;
+}
+
 // One word of codes -> the m16n8k16 A fragment of the thread: nibbles (0,4) are
 // row g columns (2t, 2t+1), (1,5) row g+8 columns (2t, 2t+1), (2,6) row g
 // columns (2t+8, 2t+9), (3,7) row g+8 columns (2t+8, 2t+9).  (1024 + q) and
@@ -236,6 +252,16 @@ __device__ __forceinline__ GfRows gf_rows(uint32_t vx, uint32_t vy) {
   k.z_lo = -a.x * a.y;
   k.s_hi = b.x * 0.0625f;
   k.z_hi = -b.x * b.y;
+  return k;
+}
+// Affine format: the term of the activation sum is the bias itself (b sum(x)).
+__device__ __forceinline__ GfRows gf_rows_affine(uint32_t vx, uint32_t vy) {
+  const float2 a = __half22float2(bits_h2(vx)), b = __half22float2(bits_h2(vy));
+  GfRows k;
+  k.s_lo = a.x;
+  k.z_lo = a.y;
+  k.s_hi = b.x * 0.0625f;
+  k.z_hi = b.y;
   return k;
 }
 
@@ -320,7 +346,7 @@ __device__ __forceinline__ bool read_item(const MmHeader& H, int i, const MmArgs
 
 // One stage of one compute warp: KK 16-column steps, NT tiles of 8 tokens, groups of G,
 // for the warp's two strips 2 sw and 2 sw + 1 (one token fragment serves both).
-template <int NT, int G, int KK>
+template <int NT, int G, int KK, bool AF>
 __device__ __forceinline__ bool run_stage(const MmArgs& a, MmHeader& H, volatile int* abort,
                                           float (&acc)[2][NT][4], int& slot, uint32_t& phase, uint32_t ring_s,
                                           const uint32_t (&loff)[4], int sw, int lane) {
@@ -359,7 +385,8 @@ __device__ __forceinline__ bool run_stage(const MmArgs& a, MmHeader& H, volatile
     if (kk % kStepsPerGroup == 0)
 #pragma unroll
       for (int h = 0; h < 2; ++h)
-        k[h] = dq_rows(szw[h][2 * (kk / kStepsPerGroup)], szw[h][2 * (kk / kStepsPerGroup) + 1]);
+        k[h] = AF ? dq_rows_affine(szw[h][2 * (kk / kStepsPerGroup)], szw[h][2 * (kk / kStepsPerGroup) + 1])
+                  : dq_rows(szw[h][2 * (kk / kStepsPerGroup)], szw[h][2 * (kk / kStepsPerGroup) + 1]);
     uint32_t af[2][4];
     dequant_frag(words[0][kk % 4], k[0], af[0]);
     dequant_frag(words[1][kk % 4], k[1], af[1]);
@@ -401,7 +428,7 @@ __device__ __forceinline__ bool run_stage(const MmArgs& a, MmHeader& H, volatile
 // two 8-column halves) form the m16k16 A fragment {b0, b2, b1, b3}, times a B
 // fragment of 2^-24, so that row m of the result is token m's sum; four shuffles
 // move those into the accumulators' token columns.
-template <int NT, int G, int KK>
+template <int NT, int G, int KK, bool AF>
 __device__ __forceinline__ bool run_stage_gf(const MmArgs& a, MmHeader& H, volatile int* abort,
                                              float (&tot)[2][NT][4], int& slot, uint32_t& phase, uint32_t ring_s,
                                              const uint32_t (&loff)[4], int sw, int lane) {
@@ -471,7 +498,7 @@ __device__ __forceinline__ bool run_stage_gf(const MmArgs& a, MmHeader& H, volat
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const GfRows k = gf_rows(szw[h][2 * j], szw[h][2 * j + 1]);
+      const GfRows k = AF ? gf_rows_affine(szw[h][2 * j], szw[h][2 * j + 1]) : gf_rows(szw[h][2 * j], szw[h][2 * j + 1]);
 #pragma unroll
       for (int u = 0; u < NT; ++u) {
         float(&t)[4] = tot[h][u];
@@ -493,7 +520,7 @@ __device__ __forceinline__ bool run_stage_gf(const MmArgs& a, MmHeader& H, volat
 
 // One item of one compute warp: every stage of the contraction, then the epilogue.
 // Returns false if a wait gave up.
-template <int NT, int G, bool GF>
+template <int NT, int G, bool GF, bool AF>
 __device__ __forceinline__ bool run_item(const MmArgs& a, MmHeader& H, volatile int* abort, const ItemView& v,
                                          int& slot, uint32_t& phase, uint32_t ring_s, const uint32_t (&loff)[4],
                                          int sw, int lane) {
@@ -509,14 +536,14 @@ __device__ __forceinline__ bool run_item(const MmArgs& a, MmHeader& H, volatile 
   constexpr int G4 = G < 64 ? G : 64;  // groups of the last 64 columns
   if constexpr (GF) {
     for (int c0 = 0; c0 + kStageCols <= K; c0 += kStageCols)
-      if (!run_stage_gf<NT, G, 8>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
+      if (!run_stage_gf<NT, G, 8, AF>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
     if (G < 128 && (K % kStageCols) != 0)
-      if (!run_stage_gf<NT, G4, 4>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
+      if (!run_stage_gf<NT, G4, 4, AF>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
   } else {
     for (int c0 = 0; c0 + kStageCols <= K; c0 += kStageCols)
-      if (!run_stage<NT, G, 8>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
+      if (!run_stage<NT, G, 8, AF>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
     if (G < 128 && (K % kStageCols) != 0)  // the last 64 columns
-      if (!run_stage<NT, G4, 4>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
+      if (!run_stage<NT, G4, 4, AF>(a, H, abort, acc, slot, phase, ring_s, loff, sw, lane)) return false;
   }
   if constexpr (GF) {
 #pragma unroll
@@ -574,25 +601,26 @@ __device__ __forceinline__ bool run_item(const MmArgs& a, MmHeader& H, volatile 
   return true;
 }
 
-template <int G, bool GF>
+template <int G, bool GF, bool AF>
 __device__ __forceinline__ bool run_item_g(const MmArgs& a, MmHeader& H, volatile int* abort, const ItemView& v,
                                            int& slot, uint32_t& phase, uint32_t ring_s, const uint32_t (&loff)[4],
                                            int sw, int lane) {
   const int nt = (v.n_cnt + 7) / 8;
   if constexpr (GF)  // items of at most kChunkGf tokens
-    return nt == 1 ? run_item<1, G, true>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
-                   : run_item<2, G, true>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+    return nt == 1 ? run_item<1, G, true, AF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
+                   : run_item<2, G, true, AF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
   switch (nt) {
-    case 1: return run_item<1, G, false>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
-    case 2: return run_item<2, G, false>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
-    case 3: return run_item<3, G, false>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
-    default: return run_item<4, G, false>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+    case 1: return run_item<1, G, false, AF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+    case 2: return run_item<2, G, false, AF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+    case 3: return run_item<3, G, false, AF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+    default: return run_item<4, G, false, AF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
   }
 }
 
-// GF: the group-factorised reduction order (its own instantiation, so that each
-// order gets its own register allocation).
-template <bool GF>
+// GF: the group-factorised reduction order; AF: the affine weight format (its own
+// instantiations, so that each gets its own register allocation; the symmetric
+// format is the asymmetric one with every zero-point 8).
+template <bool GF, bool AF>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     expert_gemm_mma_kernel(const MmArgs a, const __grid_constant__ CUtensorMap map_x,
                            const __grid_constant__ CUtensorMap map_h) {
@@ -739,9 +767,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (!warp_wait(smem_addr(&H.item_full[i % kQueue]), (i / kQueue) & 1, a, abort)) break;
       ItemView v;
       if (!read_item(H, i, a, v)) break;
-      const bool ok = v.g == 32   ? run_item_g<32, GF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
-                      : v.g == 64 ? run_item_g<64, GF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
-                                  : run_item_g<128, GF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
+      const bool ok = v.g == 32   ? run_item_g<32, GF, AF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
+                      : v.g == 64 ? run_item_g<64, GF, AF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane)
+                                  : run_item_g<128, GF, AF>(a, H, abort, v, slot, phase, ring_s, loff, sw, lane);
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&H.item_empty[i % kQueue]));
@@ -836,8 +864,10 @@ bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
 }  // namespace
 
 cudaError_t init_gemm_kernels(int* blocks_per_sm) {
-  for (const void* fn : {reinterpret_cast<const void*>(expert_gemm_mma_kernel<false>),
-                         reinterpret_cast<const void*>(expert_gemm_mma_kernel<true>)}) {
+  for (const void* fn : {reinterpret_cast<const void*>(expert_gemm_mma_kernel<false, false>),
+                         reinterpret_cast<const void*>(expert_gemm_mma_kernel<true, false>),
+                         reinterpret_cast<const void*>(expert_gemm_mma_kernel<false, true>),
+                         reinterpret_cast<const void*>(expert_gemm_mma_kernel<true, true>)}) {
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
@@ -892,8 +922,9 @@ cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, cons
   }
   CUtensorMap map_x, map_h;
   if (!make_row_map(&map_x, ws.xs, P, s.d) || !make_row_map(&map_h, ws.h, P, s.f)) return cudaErrorInvalidValue;
-  return s.red ? launch_pdl(expert_gemm_mma_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, st, a, map_x, map_h)
-               : launch_pdl(expert_gemm_mma_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, st, a, map_x, map_h);
+  auto* kern = s.fmt == 1 ? (s.red ? expert_gemm_mma_kernel<true, true> : expert_gemm_mma_kernel<false, true>)
+                          : (s.red ? expert_gemm_mma_kernel<true, false> : expert_gemm_mma_kernel<false, false>);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, st, a, map_x, map_h);
 }
 
 }  // namespace moe

@@ -33,7 +33,7 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
 struct Dims {
-  int T, d, f, E, k, g1, g2, act, red;
+  int T, d, f, E, k, g1, g2, act, red, fmt;
   int64_t pairs() const { return int64_t(T) * k; }
 };
 

@@ -166,12 +166,18 @@ moe_w4a16_status moe_w4a16_prepare(const moe_w4a16_shape* shape, int32_t which, 
   if (!shape) return MOE_W4A16_ERR_NULL;
   Proj p;
   if (!proj_of(shape, which, &p)) return MOE_W4A16_ERR_SHAPE;
-  if (!q || !scale || !zero || !out) return MOE_W4A16_ERR_NULL;
+  const int fmt = shape->format;
+  if (!q || !scale || !out || (!zero && fmt != 2)) return MOE_W4A16_ERR_NULL;
   const int64_t nsz = p.E * p.R * (p.K / p.g);
+  std::vector<uint16_t> eights;
+  if (fmt == 2) {  // symmetric: the zero-point slot holds 8 (0x4800), whatever zero points to
+    eights.assign(size_t(nsz), uint16_t(0x4800));
+    zero = eights.data();
+  }
   for (int64_t i = 0; i < nsz; ++i) {
     const double s = half_value(scale[i]), z = half_value(zero[i]);
     if (!std::isfinite(s) || std::fabs(s) > 32.0) return MOE_W4A16_ERR_VALUE;
-    if (!(z >= 0.0 && z <= 16.0)) return MOE_W4A16_ERR_VALUE;
+    if (fmt == 1 ? !(std::fabs(z) <= 1024.0) : !(z >= 0.0 && z <= 16.0)) return MOE_W4A16_ERR_VALUE;
   }
   return walk<true>(p, const_cast<uint8_t*>(q), const_cast<uint16_t*>(scale), const_cast<uint16_t*>(zero), out);
 }
@@ -181,8 +187,13 @@ moe_w4a16_status moe_w4a16_unprepare(const moe_w4a16_shape* shape, int32_t which
   if (!shape) return MOE_W4A16_ERR_NULL;
   Proj p;
   if (!proj_of(shape, which, &p)) return MOE_W4A16_ERR_SHAPE;
-  if (!prepared || !q || !scale || !zero) return MOE_W4A16_ERR_NULL;
+  if (!prepared || !q || !scale || (!zero && shape->format != 2)) return MOE_W4A16_ERR_NULL;
   std::memset(q, 0, size_t(p.E * p.R * (p.K / 2)));
+  std::vector<uint16_t> scratch;
+  if (!zero) {  // symmetric format without a zero-point array
+    scratch.resize(size_t(p.E * p.R * (p.K / p.g)));
+    zero = scratch.data();
+  }
   return walk<false>(p, q, scale, zero, const_cast<uint8_t*>(prepared));
 }
 

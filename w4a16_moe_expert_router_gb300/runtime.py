@@ -17,7 +17,7 @@ from .synth import Workload
 
 def shape_of(wl: Workload, tokens: int | None = None) -> B.Shape:
     return B.make_shape(wl.tokens if tokens is None else tokens, wl.hidden, wl.inter, wl.experts, wl.top_k,
-                        wl.group_gate_up, wl.group_down, wl.activation, wl.reduction)
+                        wl.group_gate_up, wl.group_down, wl.activation, wl.reduction, wl.format)
 
 
 @dataclass
