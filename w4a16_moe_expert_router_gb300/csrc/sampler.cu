@@ -313,52 +313,79 @@ __global__ void __launch_bounds__(kFinalThreads)
     sample_final_kernel(const Partial* __restrict__ part, int P, int S, int rule, float bound,
                         const uint8_t* __restrict__ revealed, int32_t* __restrict__ token, float* __restrict__ entropy,
                         float* __restrict__ pmax, uint8_t* __restrict__ accept) {
-  __shared__ float sh_h[kFinalThreads], sh_pm[kFinalThreads], sorted_h[kFinalThreads];
-  __shared__ int sorted_p[kFinalThreads];
-  __shared__ uint8_t sh_rev[kFinalThreads], sh_acc[kFinalThreads];
+  __shared__ __align__(16) float sh_h[kFinalThreads];
+  __shared__ __align__(16) float sh_pm[kFinalThreads];
+  __shared__ __align__(16) float sorted_h[kFinalThreads];
+  __shared__ __align__(16) int sorted_p[kFinalThreads];
+  __shared__ __align__(16) uint8_t sh_rev[kFinalThreads];
+  __shared__ uint8_t sh_acc[kFinalThreads];
   const int p = threadIdx.x;
+  // positions past P take part as revealed, with an entropy that ranks last
+  float h = INFINITY, pm = 0.f;
+  uint8_t rev = 1;
   if (p < P) {
-    const Partial* q = part + static_cast<int64_t>(p) * S;
-    float m2 = q[0].m2, z = q[0].z, s1 = q[0].s1, bk = q[0].key;
-    int32_t bv = q[0].v;
+    const float4* q = reinterpret_cast<const float4*>(part + static_cast<int64_t>(p) * S);
+    float4 a = __ldg(q);
+    float m2 = a.x, z = a.y, s1 = a.z, bk = a.w;
+    int32_t bv = __float_as_int(__ldg(q + 1).x);
     for (int i = 1; i < S; ++i) {
-      merge_sums(m2, z, s1, q[i].m2, q[i].z, q[i].s1);
-      if (better(q[i].key, q[i].v, bk, bv)) {
-        bk = q[i].key;
-        bv = q[i].v;
+      const float4 b = __ldg(q + 2 * i);
+      const int32_t v = __float_as_int(__ldg(q + 2 * i + 1).x);
+      merge_sums(m2, z, s1, b.x, b.y, b.z);
+      if (better(b.w, v, bk, bv)) {
+        bk = b.w;
+        bv = v;
       }
     }
-    const float h = logf(z) - (s1 / z) * 0.693147180559945309f;
-    const float pm = 1.f / z;
+    h = logf(z) - (s1 / z) * 0.693147180559945309f;
+    pm = 1.f / z;
+    rev = revealed[p] != 0;
     token[p] = bv;
     entropy[p] = h;
     pmax[p] = pm;
-    sh_h[p] = h;
-    sh_pm[p] = pm;
-    sh_rev[p] = revealed[p] != 0;
-    sh_acc[p] = 0;
   }
-  __syncthreads();
+  sh_h[p] = h;
+  sh_pm[p] = pm;
+  sh_rev[p] = rev;
+  sh_acc[p] = 0;
+  const int n = __syncthreads_count(!rev);  // unrevealed positions
+  const int P4 = (P + 3) & ~3;              // rank over whole float4s: padded slots are revealed
   if (rule == 0) {
     // rank of each unrevealed position by (entropy, position)
-    if (p < P && !sh_rev[p]) {
-      const float h = sh_h[p];
+    if (!rev) {
       int r = 0;
-      for (int q = 0; q < P; ++q)
-        if (!sh_rev[q] && (sh_h[q] < h || (sh_h[q] == h && q < p))) ++r;
+      for (int q = 0; q < P4; q += 4) {
+        const float4 hq = *reinterpret_cast<const float4*>(&sh_h[q]);
+        const uchar4 rq = *reinterpret_cast<const uchar4*>(&sh_rev[q]);
+        r += !rq.x && (hq.x < h || (hq.x == h && q < p));
+        r += !rq.y && (hq.y < h || (hq.y == h && q + 1 < p));
+        r += !rq.z && (hq.z < h || (hq.z == h && q + 2 < p));
+        r += !rq.w && (hq.w < h || (hq.w == h && q + 3 < p));
+      }
       sorted_h[r] = h;
       sorted_p[r] = p;
     }
     __syncthreads();
     if (p == 0) {
-      int n = 0;
-      for (int q = 0; q < P; ++q) n += !sh_rev[q];
+      // the mlx-vlm rule in sorted order, one fp32 rounding per step, in sequence
       float c = 0.f, x = -INFINITY;
-      for (int i = 0; i < n; ++i) {
+      int i = 0;
+      for (; i + 4 <= n; i += 4) {
+        const float4 hv = *reinterpret_cast<const float4*>(&sorted_h[i]);
+        const int4 pv = *reinterpret_cast<const int4*>(&sorted_p[i]);
+        const float hh[4] = {hv.x, hv.y, hv.z, hv.w};
+        const int pp[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          c = __fadd_rn(c, hh[u]);
+          x = fmaxf(x, hh[u]);
+          if (i + u == 0 || __fsub_rn(c, x) <= bound) sh_acc[pp[u]] = 1;
+        }
+      }
+      for (; i < n; ++i) {
         c = __fadd_rn(c, sorted_h[i]);
         x = fmaxf(x, sorted_h[i]);
-        const float d = __fsub_rn(c, x);
-        if (i == 0 || d <= bound) sh_acc[sorted_p[i]] = 1;
+        if (i == 0 || __fsub_rn(c, x) <= bound) sh_acc[sorted_p[i]] = 1;
       }
     }
   } else if (p == 0) {
