@@ -474,8 +474,7 @@ def run_sampler(args):
     libbuild.build()
     P, V, seed = 256, 262144, 1234
     steps, warmup = min(args.steps, 2000), max(3, min(args.warmup, 20))
-    rng = np.random.default_rng(0)
-    host = [(rng.standard_normal((P, V), dtype=np.float32) * 3.0) for _ in range(2)]
+    host = sampler_logits(P, V)
     dev = [torch.from_numpy(h).cuda() for h in host]
     revealed = torch.zeros(P, dtype=torch.uint8, device="cuda")
     tok = torch.empty(P, dtype=torch.int32, device="cuda")
@@ -558,9 +557,52 @@ def run_sampler(args):
     return res
 
 
+def sampler_logits(P, V, copies=2):
+    """The sampler workload's fp32 logits: 3 N(0, 1), one array per alternating copy."""
+    import numpy as np
+    rng = np.random.default_rng(0)
+    return [(rng.standard_normal((P, V), dtype=np.float32) * 3.0) for _ in range(copies)]
+
+
+def run_sampler_reference(args):
+    """The sampler oracle as it stands on the host cores: each step a bounded sample of
+    the workload's positions (fp64 entropy and the Gumbel keys of every token),
+    scaled to steps/s of the full 256-position step."""
+    import oracle
+    P, V, seed = 256, 262144, 1234
+    nth = os.cpu_count() or 1
+    lg = sampler_logits(P, V, copies=1)[0]
+    sample_p = max(1, min(P, nth * 2))
+    for i in range(min(args.warmup, 1)):
+        oracle.sample(lg[:sample_p], 1.0, seed, i, nthreads=nth)
+    budget_s, t0, done, spent = 120.0, time.perf_counter(), 0, 0.0
+    for i in range(args.steps):
+        t = time.perf_counter()
+        oracle.sample(lg[(i * sample_p) % P:][:sample_p], 1.0, seed, i, nthreads=nth)
+        spent += (time.perf_counter() - t) * P / sample_p
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    value = done / spent
+    return {
+        "impl": "reference", "metric": SAMPLER_METRIC, "value": value, "unit": "steps/s", "n_gpus": 1,
+        "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 * spent / done, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "sampler_p256_v262144", "positions": P, "vocab": V, "logits": "3 * N(0, 1) fp32",
+                   "rule": "entropy bound 40"},
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": nth, "kind": "oracle",
+                         "sample": f"{sample_p} of the {P} positions per step, {nth} threads, scaled to a full step"},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.sampler:
+        if args.impl == "reference":
+            if int(os.environ.get("RANK", "0")) == 0:
+                print(json.dumps(run_sampler_reference(args)), flush=True)
+            return
         print(json.dumps(run_sampler(args)), flush=True)
         return
     if args.impl == "reference":
