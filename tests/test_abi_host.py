@@ -265,3 +265,19 @@ def test_prepare_per_format():
                                   np.full_like(ws["down_zero"], 0x4800))
     assert np.array_equal(p_none, p_any) and np.array_equal(p_none, p_eight)
     assert prep.nbytes == B.moe_w4a16_prepared_bytes(sh, B.GATE_UP)
+
+
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_prepare_unprepare_round_trip_per_format(fmt):
+    """The stream keeps the affine bias unchanged, and the symmetric format's zero slot
+    reads back as 8 whatever zero array was (or was not) given."""
+    import dataclasses
+    wl = dataclasses.replace(synth.WORKLOADS["tiny"], format=fmt)
+    w = synth.make_weights(wl, 5)
+    sh = runtime.shape_of(wl)
+    for which, (q, s, z) in ((B.GATE_UP, ("gate_up_q", "gate_up_scale", "gate_up_zero")),
+                             (B.DOWN, ("down_q", "down_scale", "down_zero"))):
+        prep = B.moe_w4a16_prepare(sh, which, w[q], w[s], None if fmt == 2 else w[z])
+        q2, s2, z2 = B.moe_w4a16_unprepare(sh, which, prep, w[q].shape, w[s].shape)
+        assert np.array_equal(q2, w[q]) and np.array_equal(s2, w[s])
+        assert np.array_equal(z2, w[z] if fmt == 1 else np.full_like(w[z], 0x4800))
