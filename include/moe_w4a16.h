@@ -8,15 +8,21 @@
  *               logits; the k selected logits are softmax-normalised;
  *   2. expert:  each (token, expert) pair runs the expert's gated-GELU FFN
  *               h = gelu(Wg x) * (Wu x),  y = Wd h,  with Wg|Wu|Wd stored as
- *               asymmetric uint4 codes with an fp16 scale and zero-point per
- *               group along the contraction dim, w = (q - z) * s, dequantised
- *               inside the GEMM ("the kernels we built": the GEMM reads packed
- *               nibbles and dequantises inline);
+ *               uint4 codes with an fp16 scale and a second fp16 value per
+ *               group along the contraction dim -- by default asymmetric,
+ *               w = (q - z) * s; affine w = q * s + b and symmetric
+ *               w = (q - 8) * s are selectable (moe_w4a16_shape.format) --
+ *               dequantised inside the GEMM ("the kernels we built": the GEMM
+ *               reads packed nibbles and dequantises inline), in one of two
+ *               reduction orders (moe_w4a16_shape.reduction);
  *   3. combine: out[t] = sum over router ranks r = 0..k-1, in rank order, of
  *               w[t][r] * y[t][r], in fp32 with no atomics ("the kernels we
  *               built": fixed-order combine instead of index_add_), optionally
  *               followed by an fp32 RMSNorm ("the kernels we built": fused
  *               RMSNorm).
+ * Beside the layer, moe_w4a16_sample runs the per-step sampler of the
+ * denoising loop (entropy, Gumbel-max token, acceptance of positions) in one
+ * streaming pass over the vocabulary logits (see its section below).
  * The weight format follows the model card's "requirements" paragraph
  * (dg-w4a16-v1: two nibbles per byte; gate_up_proj grouped along the
  * contraction dim; down_proj grouped at 64 because its contraction dim, 704, is
@@ -33,7 +39,8 @@
  *     validate it: out-of-range device contents (e.g. an expert id >= E in a
  *     caller-built routing) are the caller's responsibility.
  *   - fp16 values travel as uint16_t bit patterns (IEEE binary16).
- *   - Every device pointer must be 16-byte aligned.
+ *   - Every device pointer of the layer's calls must be 16-byte aligned (the
+ *     sampler's rules are in its section).
  *   - Calls sharing one workspace must not overlap in time (same stream, or
  *     ordered by events); calls with separate workspaces are independent.
  *   - Results are bit-identical from run to run for the same inputs and shape:
