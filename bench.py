@@ -430,7 +430,6 @@ def run_reference(args, rank, world):
     """The oracle as it stands, one token of the canvas per step, on the host cores."""
     if rank != 0:
         return None
-    from w4a16_moe_expert_router_gb300 import synth
     wl = workload_of(args)
     nth = os.cpu_count() or 1
     case = OracleCase(wl)
@@ -467,7 +466,6 @@ def run_sampler(args):
     """K sampler calls on device-resident logits (two 268 MB copies alternate, each
     larger than L2), CUDA events on the launching stream; then the same call end to
     end with the logits copied in from pinned host memory and the outputs read back."""
-    import numpy as np
     import torch
     from w4a16_moe_expert_router_gb300 import binding as B
     from w4a16_moe_expert_router_gb300 import build as libbuild
