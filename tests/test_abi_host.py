@@ -281,3 +281,33 @@ def test_prepare_unprepare_round_trip_per_format(fmt):
         q2, s2, z2 = B.moe_w4a16_unprepare(sh, which, prep, w[q].shape, w[s].shape)
         assert np.array_equal(q2, w[q]) and np.array_equal(s2, w[s])
         assert np.array_equal(z2, w[z] if fmt == 1 else np.full_like(w[z], 0x4800))
+
+
+def test_ctypes_structs_match_the_header(tmp_path):
+    """The binding's ctypes structures have the sizes and field offsets the C compiler
+    gives the header's structs (a program built with gcc against include/moe_w4a16.h)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    structs = {"moe_w4a16_shape": B.Shape, "moe_w4a16_sampler": B.Sampler, "moe_w4a16_weights": B.Weights,
+               "moe_w4a16_routing": B.Routing}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "moe_w4a16.h"', "int main(void) {"]
+    for cname, cls in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for field, _ in cls._fields_:
+            lines.append(f'  printf("{cname} {field} %zu\\n", offsetof({cname}, {field}));')
+    lines.append("  return 0;\n}")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    include = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run(["gcc", "-std=c11", "-I", include, str(src), "-o", str(exe)], check=True)
+    got = {}
+    for ln in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        name, field, val = ln.split()
+        got[(name, field)] = int(val)
+    for cname, cls in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(cls), cname
+        for field, _ in cls._fields_:
+            assert got[(cname, field)] == getattr(cls, field).offset, (cname, field)
