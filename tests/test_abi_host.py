@@ -311,3 +311,27 @@ def test_ctypes_structs_match_the_header(tmp_path):
         assert got[(cname, "size")] == ctypes.sizeof(cls), cname
         for field, _ in cls._fields_:
             assert got[(cname, field)] == getattr(cls, field).offset, (cname, field)
+
+
+def test_smoke_sampler_check_with_a_host_stand_in():
+    """The sampler part of __graft_entry__.smoke() run on the CPU, with a stand-in for
+    the GPU call that writes the oracle's own outputs: the check's marshalling and
+    comparisons are exercised here; on a GPU the real call takes the stand-in's place."""
+    import types
+    import torch
+    import oracle
+    import __graft_entry__ as ge
+
+    def fake_sample(cfg, logits, revealed, token, entropy, pmax, accept, workspace, stream=None):
+        lg = logits.cpu().numpy()
+        t, e, pm = oracle.sample(lg, cfg.inv_temperature, cfg.seed, cfg.step)
+        token.copy_(torch.from_numpy(t))
+        entropy.copy_(torch.from_numpy(e.astype(np.float32)))
+        pmax.copy_(torch.from_numpy(pm.astype(np.float32)))
+        acc = oracle.accept_entropy(e.astype(np.float32), revealed.cpu().numpy(), cfg.bound)
+        accept.copy_(torch.from_numpy(acc))
+
+    stand_in = types.SimpleNamespace(make_sampler=B.make_sampler,
+                                     moe_w4a16_sampler_workspace_bytes=B.moe_w4a16_sampler_workspace_bytes,
+                                     moe_w4a16_sample=fake_sample)
+    assert ge._smoke_sampler(stand_in, device="cpu") <= 1e-6
