@@ -294,8 +294,10 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_unprepare(const moe_w4a16_shape* shape,
  *
  * moe_w4a16_forward_noalloc computes exactly what moe_w4a16_forward computes
  * (the gate_up and down GEMMs and the combine, on a routing written by
- * moe_w4a16_route), but keeps its scratch memory in a static device array built
- * into the library instead of a caller-provided workspace, and allocates nothing.
+ * moe_w4a16_route; the same shape rules, reduction orders and weight formats,
+ * and bit-identical outputs), but keeps its scratch memory in a static device
+ * array built into the library instead of a caller-provided workspace, and
+ * allocates nothing.
  * The pages describe no counterpart to this call; it exists for callers that
  * cannot obtain device memory of their own -- for example a plugin running
  * inside a host application whose memory manager owns the whole device heap
@@ -326,7 +328,6 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_forward_noalloc(const moe_w4a16_shape* 
                                                          const moe_w4a16_weights* weights, const float* norm_gamma,
                                                          float norm_eps, uint16_t* out, void* stream);
 
-/* Static description of a status code (never NULL). */
 /* Self-test of the device-side failure path.  Every wait in the expert launch
  * (on its mbarrier rings and on the counters other CTAs raise) is bounded: on
  * expiry the kernel records MOE_W4A16_ERR_TIMEOUT in the workspace's error
@@ -340,6 +341,7 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_forward_noalloc(const moe_w4a16_shape* 
 MOE_W4A16_API moe_w4a16_status moe_w4a16_selftest_wait_timeout(void* workspace, size_t workspace_bytes,
                                                                uint64_t limit_ns, void* stream);
 
+/* Static description of a status code (never NULL). */
 MOE_W4A16_API const char* moe_w4a16_status_string(moe_w4a16_status status);
 
 #ifdef __cplusplus

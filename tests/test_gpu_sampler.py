@@ -115,6 +115,17 @@ def test_sampler_full_canvas_step(B, rule, bound):
     assert outs[0][3].sum() >= 1
 
 
+@pytest.mark.parametrize("rule,bound", [(0, 60.0), (1, 0.4)])
+def test_sampler_max_positions(B, rule, bound):
+    """P = 1024, the most positions one call takes (the final CTA holds one position
+    per thread), over 16,384 tokens; every position checked."""
+    P, V = 1024, 16384
+    lg = _logits(P, V, 3.0, seed=1024 + rule)
+    revealed = (np.arange(P) % 7 == 2).astype(np.uint8)
+    (got,) = _gpu_sample(B, lg, revealed, 1.0, rule, bound, seed=4242, step=11)
+    _check(lg, revealed, 1.0, rule, bound, 4242, 11, got)
+
+
 def test_sampler_all_revealed_accepts_nothing(B):
     P, V = 4, 4096
     lg = _logits(P, V, 1.0, 5)

@@ -57,6 +57,11 @@ def build(verbose: bool = False) -> str:
     os.makedirs(LIB_DIR, exist_ok=True)
     newest = max(os.path.getmtime(h) for h in _headers())
     srcs = _sources()
+    # objects of sources that no longer exist are removed, so the link never sees them
+    live = {os.path.basename(src) + ".o" for src in srcs}
+    for obj in glob.glob(os.path.join(OBJ_DIR, "*.o")):
+        if os.path.basename(obj) not in live:
+            os.remove(obj)
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(lambda s: _compile(s, newest, verbose), srcs))
     if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):

@@ -10,15 +10,10 @@
 #include "internal.h"
 #include "moe_w4a16.h"
 
-namespace {
-
-using moe::Dims;
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-bool pow2_group(int g) { return g == 32 || g == 64 || g == 128; }
+namespace moe {
 
 moe_w4a16_status check_shape(const moe_w4a16_shape* sh, Dims* out) {
+  const auto pow2_group = [](int g) { return g == 32 || g == 64 || g == 128; };
   if (!sh) return MOE_W4A16_ERR_NULL;
   const Dims s{sh->tokens, sh->hidden, sh->inter, sh->experts, sh->top_k, sh->group_gate_up, sh->group_down,
                sh->activation, sh->reduction, sh->format};
@@ -36,6 +31,15 @@ moe_w4a16_status check_shape(const moe_w4a16_shape* sh, Dims* out) {
   if (out) *out = s;
   return MOE_W4A16_OK;
 }
+
+}  // namespace moe
+
+namespace {
+
+using moe::check_shape;
+using moe::Dims;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Per-device state: checked compute capability, kernel attributes, SM count.
 struct DeviceState {
@@ -171,6 +175,7 @@ struct FwdArgs {
   void* ws;
   size_t ws_bytes;
   void* stream;
+  bool clear_header;  // clear the workspace header (error word, work counters) before the launches
 };
 
 // Validates what the requested steps read and write, then launches them in order.
@@ -200,6 +205,8 @@ moe_w4a16_status run_forward_steps(const moe_w4a16_shape* shape, int steps, cons
   const moe::GemmWorkspace ws = moe::carve_workspace(a.ws, s);
   const auto cs = static_cast<cudaStream_t>(a.stream);
   const int grid = dev->num_sms * dev->gemm_blocks_per_sm;
+  if (a.clear_header && cudaMemsetAsync(ws.hdr, 0, sizeof(moe::WsHeader), cs) != cudaSuccess)
+    return MOE_W4A16_ERR_CUDA;
   // gate_up and down together run as one launch (down items wait for their expert's h rows)
   const int gemm = ((steps & kGateUp) ? moe::kGemmGateUp : 0) | ((steps & kDown) ? moe::kGemmDown : 0);
   if (gemm && moe::launch_expert_gemm(gemm, s, a.x, r.expert_offsets, r.pair_list,
@@ -213,41 +220,50 @@ moe_w4a16_status run_forward_steps(const moe_w4a16_shape* shape, int steps, cons
 
 }  // namespace
 
+moe_w4a16_status moe::forward_all_steps(const moe_w4a16_shape* shape, const uint16_t* x,
+                                        const moe_w4a16_routing* routing, const moe_w4a16_weights* weights,
+                                        const float* norm_gamma, float norm_eps, uint16_t* out, void* workspace,
+                                        size_t workspace_bytes, void* stream, bool clear_header) {
+  return run_forward_steps(shape, kGateUp | kDown | kCombine,
+                           FwdArgs{x, routing, weights, norm_gamma, norm_eps, out, workspace, workspace_bytes, stream,
+                                   clear_header});
+}
+
 extern "C" {
 
 moe_w4a16_status moe_w4a16_forward(const moe_w4a16_shape* shape, const uint16_t* x, const moe_w4a16_routing* routing,
                                    const moe_w4a16_weights* weights, const float* norm_gamma, float norm_eps,
                                    uint16_t* out, void* workspace, size_t workspace_bytes, void* stream) {
   return run_forward_steps(shape, kGateUp | kDown | kCombine,
-                           FwdArgs{x, routing, weights, norm_gamma, norm_eps, out, workspace, workspace_bytes, stream});
+                           FwdArgs{x, routing, weights, norm_gamma, norm_eps, out, workspace, workspace_bytes, stream, false});
 }
 
 moe_w4a16_status moe_w4a16_experts(const moe_w4a16_shape* shape, const uint16_t* x, const moe_w4a16_routing* routing,
                                    const moe_w4a16_weights* weights, void* workspace, size_t workspace_bytes,
                                    void* stream) {
   return run_forward_steps(shape, kGateUp | kDown,
-                           FwdArgs{x, routing, weights, nullptr, 0.f, nullptr, workspace, workspace_bytes, stream});
+                           FwdArgs{x, routing, weights, nullptr, 0.f, nullptr, workspace, workspace_bytes, stream, false});
 }
 
 moe_w4a16_status moe_w4a16_gate_up(const moe_w4a16_shape* shape, const uint16_t* x, const moe_w4a16_routing* routing,
                                    const moe_w4a16_weights* weights, void* workspace, size_t workspace_bytes,
                                    void* stream) {
   return run_forward_steps(shape, kGateUp,
-                           FwdArgs{x, routing, weights, nullptr, 0.f, nullptr, workspace, workspace_bytes, stream});
+                           FwdArgs{x, routing, weights, nullptr, 0.f, nullptr, workspace, workspace_bytes, stream, false});
 }
 
 moe_w4a16_status moe_w4a16_down(const moe_w4a16_shape* shape, const moe_w4a16_routing* routing,
                                 const moe_w4a16_weights* weights, void* workspace, size_t workspace_bytes,
                                 void* stream) {
   return run_forward_steps(shape, kDown,
-                           FwdArgs{nullptr, routing, weights, nullptr, 0.f, nullptr, workspace, workspace_bytes, stream});
+                           FwdArgs{nullptr, routing, weights, nullptr, 0.f, nullptr, workspace, workspace_bytes, stream, false});
 }
 
 moe_w4a16_status moe_w4a16_combine(const moe_w4a16_shape* shape, const moe_w4a16_routing* routing,
                                    const float* norm_gamma, float norm_eps, uint16_t* out, void* workspace,
                                    size_t workspace_bytes, void* stream) {
   return run_forward_steps(shape, kCombine, FwdArgs{nullptr, routing, nullptr, norm_gamma, norm_eps, out, workspace,
-                                                    workspace_bytes, stream});
+                                                    workspace_bytes, stream, false});
 }
 
 moe_w4a16_status moe_w4a16_read_error(const void* workspace, size_t workspace_bytes, void* stream,

@@ -37,6 +37,19 @@ struct Dims {
   int64_t pairs() const { return int64_t(T) * k; }
 };
 
+// Host-side validation of a layer shape (the rules of moe_w4a16_shape); fills *out
+// when the shape is valid.
+moe_w4a16_status check_shape(const moe_w4a16_shape* sh, Dims* out);
+
+// The whole forward pass (gate_up + down in one launch, then the combine) on the
+// given workspace, with the checks and launch sequence of moe_w4a16_forward; when
+// clear_header is set the workspace header (error word, work counters) is cleared
+// on the stream after the checks pass and before the first launch.
+moe_w4a16_status forward_all_steps(const moe_w4a16_shape* shape, const uint16_t* x, const moe_w4a16_routing* routing,
+                                   const moe_w4a16_weights* weights, const float* norm_gamma, float norm_eps,
+                                   uint16_t* out, void* workspace, size_t workspace_bytes, void* stream,
+                                   bool clear_header);
+
 // Workspace carve-up: header | per-expert gate_up counters | h | xs | y | routing scratch.
 inline size_t ws_cnt_offset() { return sizeof(WsHeader); }
 inline size_t ws_h_offset() { return ws_cnt_offset() + size_t(kMaxExperts) * 4; }
