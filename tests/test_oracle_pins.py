@@ -320,6 +320,15 @@ def test_fp16_diagnostic_mode_stays_within_rounding():
 # "ashhart/TensorFold pull 802", "Summary": symmetric GPTQ 4/128 and MLX affine 4/64
 # checkpoints next to the model card's asymmetric uint4 (format 0).
 
+def test_format_triples_worked_by_hand():
+    """Affine (negative and positive biases) and symmetric (including a negative scale
+    and an ignored second value) values worked by hand from the format definitions."""
+    rows = _rows("format_triples.txt")
+    assert {r[0] for r in rows} == {"1", "2"} and len(rows) >= 10
+    for fmt, q, sb, scb, want in rows:
+        assert oracle.dequant_format(int(q), int(sb, 16), int(scb, 16), int(fmt)) == float(want)
+
+
 def test_format_dequant_values():
     s, z, b = 0x211F, 0x47C0, 0xAC00  # fp16 0.0100021..., 7.75, -0.0625
     sv, zv, bv = (float(np.array([v], np.uint16).view(np.float16)[0]) for v in (s, z, b))

@@ -13,6 +13,8 @@ bit-exact agreement of the GPU path's independent implementation with this one.
 """
 import math
 
+import os
+
 import numpy as np
 import pytest
 
@@ -58,6 +60,20 @@ def test_log_f32_special_values():
 
 
 # ------------------------------------------------------------------ Philox
+
+def test_philox_known_answer_vectors():
+    """The generator's published known-answer vectors (golden file, with its citation):
+    a swapped output word, a wrong key schedule, a wrong multiplier or a mis-ordered
+    counter changes every one of them."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.txt")
+    with open(path) as fh:
+        rows = [ln.split() for ln in fh if ln.strip() and not ln.startswith("#")]
+    assert len(rows) >= 3
+    for r in rows:
+        v = [int(x, 16) for x in r]
+        got = oracle.philox4x32_10(np.array(v[0:4], np.uint32), np.array(v[4:6], np.uint32))
+        assert [int(w) for w in got] == v[6:10]
+
 
 def test_philox_words_are_uniform_and_counters_avalanche():
     """Counter-based: the same (counter, key) gives the same words; across counters the
