@@ -46,7 +46,6 @@ struct DeviceState {
   bool ready = false;
   moe_w4a16_status status = MOE_W4A16_OK;
   int num_sms = 0;
-  int gemm_blocks_per_sm = 1;
 };
 constexpr int kMaxDevices = 64;
 DeviceState g_dev[kMaxDevices];
@@ -68,7 +67,7 @@ moe_w4a16_status device_state(const DeviceState** out) {
       st.status = MOE_W4A16_ERR_DEVICE;
     } else {
       st.num_sms = sms;
-      st.status = moe::init_gemm_kernels(&st.gemm_blocks_per_sm) == cudaSuccess ? MOE_W4A16_OK : MOE_W4A16_ERR_CUDA;
+      st.status = moe::init_gemm_kernels() == cudaSuccess ? MOE_W4A16_OK : MOE_W4A16_ERR_CUDA;
     }
     st.ready = true;
   }
@@ -204,14 +203,13 @@ moe_w4a16_status run_forward_steps(const moe_w4a16_shape* shape, int steps, cons
   if ((st = device_state(&dev)) != MOE_W4A16_OK) return st;
   const moe::GemmWorkspace ws = moe::carve_workspace(a.ws, s);
   const auto cs = static_cast<cudaStream_t>(a.stream);
-  const int grid = dev->num_sms * dev->gemm_blocks_per_sm;
   if (a.clear_header && cudaMemsetAsync(ws.hdr, 0, sizeof(moe::WsHeader), cs) != cudaSuccess)
     return MOE_W4A16_ERR_CUDA;
   // gate_up and down together run as one launch (down items wait for their expert's h rows)
   const int gemm = ((steps & kGateUp) ? moe::kGemmGateUp : 0) | ((steps & kDown) ? moe::kGemmDown : 0);
   if (gemm && moe::launch_expert_gemm(gemm, s, a.x, r.expert_offsets, r.pair_list,
                                       (steps & kGateUp) ? a.weights->gate_up : nullptr,
-                                      (steps & kDown) ? a.weights->down : nullptr, ws, grid, cs) != cudaSuccess)
+                                      (steps & kDown) ? a.weights->down : nullptr, ws, dev->num_sms, cs) != cudaSuccess)
     return MOE_W4A16_ERR_CUDA;
   if ((steps & kCombine) && moe::launch_combine(s, r.topk_w, ws.y, a.gamma, a.eps, a.out, cs) != cudaSuccess)
     return MOE_W4A16_ERR_CUDA;

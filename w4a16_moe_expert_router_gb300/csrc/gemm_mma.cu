@@ -60,6 +60,7 @@
 
 #include <mutex>
 
+#include "gemm_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -83,29 +84,14 @@ static_assert(kBBytes + kWMaxBytes <= kSlotBytes && kSlotBytes % 1024 == 0, "slo
 constexpr int kHeaderBytes = 4096;
 constexpr int kSmemBytes = 1024 + kHeaderBytes + kSlots * kSlotBytes;  // +1024 for alignment
 
-struct Proj {
-  const uint8_t* w;         // prepared stream of the projection, all experts
-  int64_t expert_bytes;     // stream bytes per expert
-  int64_t block_bytes;      // stream bytes per 128-row block
-  int nblocks;              // blocks per expert
-  int K;                    // contraction length (multiple of 64)
-  int g;                    // quantisation group along K (32, 64 or 128)
-};
 
-struct MmArgs {
-  Proj p[2];                // 0: gate_up, 1: down
-  int first, last;          // projections in this launch's work list (0 <= first <= last <= 1)
-  const int32_t* offsets;   // [E+1]
-  const int32_t* pair_list; // [T*k]
-  int E;
-  uint16_t* h;              // gate_up output, down input [T*k][f] (expert-sorted rows)
-  float* y_out;             // down output [T*k][d]
-  int f, d, act;
-  int32_t* err;
-  int32_t* counter;         // work counter of this launch
-  int32_t* done_ctas;       // CTAs that have finished; the last one resets both counters
-  int32_t* gu_done;         // [E] gate_up warps finished per expert (kMmaWarps per item)
-};
+
+using MmArgs = gemm::Args;
+using gemm::decode_item;
+using gemm::gelu;
+using gemm::kDepWaitNs;
+using gemm::tma_load_2d;
+using gemm::wait_count;
 
 // Shared-memory header (at the 1024-aligned base of dynamic shared memory).
 struct __align__(8) MmHeader {
@@ -126,40 +112,9 @@ __device__ __forceinline__ uint32_t stage_weight_bytes(int kk16, int g) {
   return static_cast<uint32_t>(kStrips * (kk16 * 128 + kSzBytesW * ng));
 }
 
-__device__ __forceinline__ int expert_of(int item, const int* prefix, int E) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {  // largest e with prefix[e] <= item
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= item) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
-}
 
-// Work item of one projection -> (expert, 128-row block, token chunk); the chunk
-// varies fastest, so concurrent items of a busy expert share weight blocks in L2.
-__device__ __forceinline__ void decode_item(int item, const int* prefix, const int* offs, int E, int chunk,
-                                            int& expert, int& blk, int& n_cnt, int& pos0) {
-  const int e = expert_of(item, prefix, E);
-  const int n_e = offs[e + 1] - offs[e];
-  const int nch = (n_e + chunk - 1) / chunk;
-  const int r = item - prefix[e];
-  const int c = r % nch;
-  expert = e;
-  blk = r / nch;
-  n_cnt = min(chunk, n_e - chunk * c);
-  pos0 = offs[e] + chunk * c;
-}
 
-constexpr uint64_t kDepWaitNs = 2000000000ull;  // bound of the wait for an expert's gate_up outputs
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
 
 // Dequantiser constants of one thread's two rows (g and g+8 of its warp's 16)
 // for one group, each broadcast to both halves of an f16x2: the zero-point split
@@ -279,53 +234,11 @@ __device__ __forceinline__ void mma_acc(float (&d)[4], const uint32_t (&a)[4], u
   }
 }
 
-__device__ __forceinline__ float gelu(float a, int act) {
-  if (act == 1) return 0.5f * a * (1.f + erff(a * 0.70710678118654752f));
-  return 0.5f * a * (1.f + tanhf(0.79788456080286536f * (a + 0.044715f * a * a * a)));
-}
 
-// Warp-uniform bounded wait: every lane polls the barrier (so each acquires the
-// phase), the warp leaves together once all lanes have seen it complete, and the
-// decision to give up is lane 0's, broadcast.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t* err, volatile int* abort,
-                                          uint64_t limit_ns = kWaitLimitNs) {
-  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity, kSuspendNs))) return true;
-    int give_up = 0;
-    if ((threadIdx.x & 31) == 0) {
-      give_up = *abort != 0;
-      if (!give_up && global_timer_ns() - t0 > limit_ns) {
-        atomicExch(err, kStatusTimeout);
-        *abort = 1;
-        give_up = 1;
-      }
-    }
-    if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
-  }
-}
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const MmArgs& a, volatile int* abort) {
-  return warp_wait(bar, parity, a.err, abort);
+  return gemm::warp_wait(bar, parity, a.err, abort);
 }
 
-// Bounded wait by one thread until a device-scope counter written by other CTAs
-// reaches need (acquire: their writes released before the count are visible).
-__device__ __forceinline__ bool wait_count(const int32_t* ctr, int need, int32_t* err, volatile int* abort,
-                                           uint64_t limit_ns) {
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-    if (v >= need) return true;
-    if (*abort || global_timer_ns() - t0 > limit_ns) {
-      atomicExch(err, kStatusTimeout);
-      *abort = 1;
-      return false;
-    }
-    __nanosleep(256);
-  }
-}
 
 // Work item as the compute warps read it from the queue.
 struct ItemView {
@@ -647,29 +560,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // everything above is set-up; the routing arrays, the row copy and h come from earlier launches
   grid_dependents_launch();
   grid_dependency_wait();
-  if (warp == 1) {  // items per expert = blocks * ceil(n_e / 32); exclusive scans, 8 experts per lane
-    for (int pj = 0; pj < 2; ++pj) {
-      const int nb = a.p[pj].nblocks;
-      int loc[8], sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int e = lane * 8 + j;
-        loc[j] = sum;
-        if (e < a.E) sum += nb * ((a.offsets[e + 1] - a.offsets[e] + kChunk - 1) / kChunk);
-      }
-      int incl = sum;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (lane * 8 + j < a.E) H.prefix[pj][lane * 8 + j] = incl - sum + loc[j];
-      if (lane == 31) H.prefix[pj][a.E] = incl;
-    }
-    for (int e = lane; e <= a.E; e += 32) H.offs[e] = a.offsets[e];
-  }
+  if (warp == 1) gemm::scan_items(a, kChunk, lane, H.prefix, H.offs);
   __syncthreads();
   // the launch's work list: [gate_up items][down items], restricted to projections first..last
   const int total0 = a.first == 0 ? H.prefix[0][a.E] : 0;
@@ -719,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
       }
-      const Proj& P = a.p[pj];
+      const gemm::Proj& P = a.p[pj];
       const CUtensorMap* bmap = pj == 0 ? &map_x : &map_h;
       const uint8_t* wsrc = P.w + static_cast<int64_t>(e) * P.expert_bytes + static_cast<int64_t>(blk) * P.block_bytes;
       for (int c0 = 0; c0 < P.K; c0 += kStageCols, ++t) {
@@ -798,13 +689,15 @@ __global__ void __launch_bounds__(32) wait_selftest_kernel(int32_t* err, const i
   }
   __syncwarp();
   volatile int* ab = &abort;
-  warp_wait(smem_addr(&bar), 0, err, ab, limit_ns);
+  gemm::warp_wait(smem_addr(&bar), 0, err, ab, limit_ns);
   __syncwarp();
   if (threadIdx.x == 0) {
     *ab = 0;  // the counter wait is timed on its own
     wait_count(flag, 1, err, ab, limit_ns);
   }
 }
+
+}  // namespace
 
 // Token rows of every (token, expert) pair, copied in expert-sorted order:
 // xs[pos] = x[pair_list[pos] / k].  One warp per row, 16-byte accesses.  Also
@@ -838,8 +731,10 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
   }
 }
 
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+}  // namespace
 
 // 2-D tensor map over rows x cols fp16 (row-major), box 64 columns x 32 rows, 128-byte swizzle.
 bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
@@ -854,16 +749,21 @@ bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
   if (!g_encode) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  const cuuint32_t box[2] = {kBoxCols, kBBoxRows};
+  const cuuint32_t box[2] = {kBoxCols, kRowBoxRows};
   const cuuint32_t estr[2] = {1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
+cudaError_t launch_gather_rows(const Dims& s, const uint16_t* x, const int32_t* pair_list, const GemmWorkspace& ws,
+                               cudaStream_t st) {
+  const int P = static_cast<int>(s.pairs());
+  return launch_pdl(gather_rows_kernel, dim3((P + 7) / 8), dim3(256), 0, st, x, pair_list, P, s.k, s.d, ws.xs,
+                    ws.gu_done, s.E);
+}
 
-cudaError_t init_gemm_kernels(int* blocks_per_sm) {
+cudaError_t init_gemm_kernels() {
   for (const void* fn : {reinterpret_cast<const void*>(expert_gemm_mma_kernel<false, false>),
                          reinterpret_cast<const void*>(expert_gemm_mma_kernel<true, false>),
                          reinterpret_cast<const void*>(expert_gemm_mma_kernel<false, true>),
@@ -873,8 +773,7 @@ cudaError_t init_gemm_kernels(int* blocks_per_sm) {
     err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (err != cudaSuccess) return err;
   }
-  *blocks_per_sm = kCtasPerSm;
-  return cudaSuccess;
+  return init_gemm_tc_kernels();
 }
 
 cudaError_t launch_wait_selftest(int32_t* err, const int32_t* flag, uint64_t limit_ns, cudaStream_t st) {
@@ -884,47 +783,21 @@ cudaError_t launch_wait_selftest(int32_t* err, const int32_t* flag, uint64_t lim
 
 cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, const int32_t* expert_offsets,
                                const int32_t* pair_list, const uint8_t* w_gate_up, const uint8_t* w_down,
-                               const GemmWorkspace& ws, int grid, cudaStream_t st) {
-  const int P = static_cast<int>(s.pairs());
-  MmArgs a{};
-  const int K[2] = {s.d, s.f}, g[2] = {s.g1, s.g2}, nb[2] = {s.f / 64, s.d / kBlockRows};
-  const uint8_t* w[2] = {w_gate_up, w_down};
-  for (int pj = 0; pj < 2; ++pj) {
-    a.p[pj].w = w[pj];
-    a.p[pj].K = K[pj];
-    a.p[pj].g = g[pj];
-    a.p[pj].nblocks = nb[pj];
-    a.p[pj].block_bytes = int64_t(kBlockRows) * K[pj] / 2 + int64_t(kBlockRows) * (K[pj] / g[pj]) * 4;
-    a.p[pj].expert_bytes = a.p[pj].block_bytes * nb[pj];
-  }
-  a.first = (which & kGemmGateUp) ? 0 : 1;
-  a.last = (which & kGemmDown) ? 1 : 0;
-  if (which == 0 || a.first > a.last) return cudaErrorInvalidValue;
-  a.offsets = expert_offsets;
-  a.pair_list = pair_list;
-  a.E = s.E;
-  a.f = s.f;
-  a.d = s.d;
-  a.act = s.act;
-  a.err = &ws.hdr->error;
-  a.h = ws.h;
-  a.y_out = ws.y;
-  // gate_up launches (alone or fused) and down-only launches keep separate counters
-  const int c = a.first == 0 ? 0 : 1;
-  a.counter = &ws.hdr->next_item[c];
-  a.done_ctas = &ws.hdr->done_ctas[c];
-  a.gu_done = ws.gu_done;
+                               const GemmWorkspace& ws, int num_sms, cudaStream_t st) {
+  MmArgs a;
+  if (!gemm::make_args(a, which, s, expert_offsets, pair_list, w_gate_up, w_down, ws)) return cudaErrorInvalidValue;
   if (which & kGemmGateUp) {
     // the token rows are first copied in expert order
-    cudaError_t err = launch_pdl(gather_rows_kernel, dim3((P + 7) / 8), dim3(256), 0, st, x, pair_list, P, s.k, s.d,
-                                 ws.xs, ws.gu_done, s.E);
+    const cudaError_t err = launch_gather_rows(s, x, pair_list, ws, st);
     if (err != cudaSuccess) return err;
   }
+  const int P = static_cast<int>(s.pairs());
   CUtensorMap map_x, map_h;
   if (!make_row_map(&map_x, ws.xs, P, s.d) || !make_row_map(&map_h, ws.h, P, s.f)) return cudaErrorInvalidValue;
-  auto* kern = s.fmt == 1 ? (s.red ? expert_gemm_mma_kernel<true, true> : expert_gemm_mma_kernel<false, true>)
-                          : (s.red ? expert_gemm_mma_kernel<true, false> : expert_gemm_mma_kernel<false, false>);
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, st, a, map_x, map_h);
+  // the per-weight order runs on the tensor-memory kernel; the group-factorised order here
+  if (s.red == 0) return launch_expert_gemm_tc(a, map_x, map_h, s.fmt == 1, num_sms, st);
+  auto* kern = s.fmt == 1 ? expert_gemm_mma_kernel<true, true> : expert_gemm_mma_kernel<true, false>;
+  return launch_pdl(kern, dim3(num_sms * kCtasPerSm), dim3(kThreads), kSmemBytes, st, a, map_x, map_h);
 }
 
 }  // namespace moe

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <utility>
@@ -17,6 +18,7 @@ constexpr int kBlockRows = 128;   // GEMM rows per work item (gate_up: 64 gate +
 constexpr int kStripRows = 16;    // GEMM rows per compute warp (one m16n8k16 row tile)
 constexpr int kStageCols = 128;   // contraction columns per pipeline stage (the last may have 64)
 constexpr int kBoxCols = 64;      // contraction columns per TMA box of token rows (128 bytes)
+constexpr int kRowBoxRows = 32;   // token rows per TMA box
 constexpr int kChunkN = 32;       // tokens (pairs) per work item
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
@@ -104,17 +106,36 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 cudaError_t launch_route(const Dims& s, const float* logits, int32_t* topk_idx, float* topk_w,
                          int32_t* expert_offsets, int32_t* pair_list, void* workspace, cudaStream_t st);
 
-// Sets the kernels' attributes on the current device and reports how many GEMM
-// CTAs fit on one SM.  Called once per device before the first launch there.
-cudaError_t init_gemm_kernels(int* blocks_per_sm);
+// Sets the GEMM kernels' attributes on the current device.  Called once per
+// device before the first launch there.
+cudaError_t init_gemm_kernels();
+cudaError_t init_gemm_tc_kernels();
 
 // Expert GEMMs.  which is a mask: kGemmGateUp (x -> h, with the copy of the
 // token rows in expert order), kGemmDown (h -> y), or both in one launch (down
-// items wait for their expert's gate_up items).
+// items wait for their expert's gate_up items).  Persistent grids sized from
+// the device's SM count.  The per-weight reduction order runs on the
+// tensor-memory kernel (gemm_tc.cu), the group-factorised order on the warp-MMA
+// kernel (gemm_mma.cu).
 constexpr int kGemmGateUp = 1, kGemmDown = 2;
 cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, const int32_t* expert_offsets,
                                const int32_t* pair_list, const uint8_t* w_gate_up, const uint8_t* w_down,
-                               const GemmWorkspace& ws, int grid, cudaStream_t st);
+                               const GemmWorkspace& ws, int num_sms, cudaStream_t st);
+
+// The expert-order copy of the token rows (the gate_up items' TMA source), which
+// also clears the per-expert gate_up counters.
+cudaError_t launch_gather_rows(const Dims& s, const uint16_t* x, const int32_t* pair_list, const GemmWorkspace& ws,
+                               cudaStream_t st);
+
+// 2-D tensor map over a rows x cols fp16 row-major matrix: boxes of 64 columns x
+// 32 rows, 128-byte swizzle.
+bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols);
+
+namespace gemm {
+struct Args;
+}
+cudaError_t launch_expert_gemm_tc(const gemm::Args& a, const CUtensorMap& map_x, const CUtensorMap& map_h, bool affine,
+                                  int num_sms, cudaStream_t st);
 
 cudaError_t launch_combine(const Dims& s, const float* topk_w, const float* y, const float* gamma, float eps,
                            uint16_t* out, cudaStream_t st);
