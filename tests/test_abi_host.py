@@ -162,11 +162,11 @@ def _check_strip(seg, ng, steps, rows, codes, scale, zero, grp0, c0):
 
 
 def test_prepared_word_layout_matches_documented_order():
-    """Group-factorised stream (reduction 1): stages of 128 columns (the last of 64
-    when K is an odd multiple of 64); per stage, eight warp strips of 16 GEMM rows;
-    gate_up strip w of block b holds gate rows 64b + 8w + (0..7) and the matching up
-    rows f + 64b + 8w + (0..7), down strip w of block b holds rows 128b + 16w + (0..15)."""
-    wl = synth.Workload("t", 4, 256, 192, 1, 1, 64, 64, reduction=1)   # d = 256 (2 stages), f = 192 (128 + 64)
+    """Stages of 128 columns (the last of 64 when K is an odd multiple of 64); per
+    stage, eight warp strips of 16 GEMM rows; gate_up strip w of block b holds gate
+    rows 64b + 8w + (0..7) and the matching up rows f + 64b + 8w + (0..7), down strip
+    w of block b holds rows 128b + 16w + (0..15)."""
+    wl = synth.Workload("t", 4, 256, 192, 1, 1, 64, 64)   # d = 256 (2 stages), f = 192 (128 + 64)
     w = synth.make_weights(wl, seed=9)
     sh = runtime.shape_of(wl)
     f = wl.inter
@@ -191,57 +191,6 @@ def test_prepared_word_layout_matches_documented_order():
         off = b * dblock + 8 * strip + wv * tail
         _check_strip(dn[off:off + tail], 1, 4, rows, dcodes, sc, ze, 2, 128)
     assert dn.nbytes == 2 * dblock
-
-
-def _tm_row(b, m, f, gate_up):
-    if not gate_up:
-        return 128 * b + m
-    q, lane = divmod(m, 32)
-    return 64 * b + 16 * q + lane if lane < 16 else f + 64 * b + 16 * q + lane - 16
-
-
-@pytest.mark.parametrize("g", [32, 64, 128])
-def test_prepared_tensor_memory_layout_matches_documented_order(g):
-    """Per-weight stream (reduction 0): per expert, per 128-row block, per stage of 128
-    columns (the last of 64 when K is an odd multiple of 64): the (scale, second) pairs
-    of the stage's groups ([group][row], 4 bytes each), then the codes
-    [quarter q][chunk c of 32 columns][lane l][word j]: row m = 32 q + l (gate_up: gate
-    row 64b + 16q + l for l < 16, up row f + 64b + 16q + l - 16 otherwise; down:
-    128b + m), word j holding columns c0 + 32 c + 8 j + (0, 2, 4, 6, 1, 3, 5, 7) in
-    nibbles 0..7."""
-    wl = synth.Workload("t", 4, 256, 192 if g < 128 else 128, 2, 1, g, g if g < 128 else 64)
-    w = synth.make_weights(wl, seed=3)
-    sh = runtime.shape_of(wl)
-    f, d = wl.inter, wl.hidden
-    order = [0, 2, 4, 6, 1, 3, 5, 7]
-    for which, (qn, sn, zn), R, K, gg, nb in (
-            (B.GATE_UP, ("gate_up_q", "gate_up_scale", "gate_up_zero"), 2 * f, d, wl.group_gate_up, f // 64),
-            (B.DOWN, ("down_q", "down_scale", "down_zero"), d, f, wl.group_down, d // 128)):
-        prep = B.moe_w4a16_prepare(sh, which, w[qn], w[sn], w[zn])
-        codes = B.moe_w4a16_unpack(w[qn].reshape(-1, K // 2)).reshape(wl.experts, R, K)
-        off = 0
-        for e in range(wl.experts):
-            for b in range(nb):
-                for c0 in range(0, K, 128):
-                    width = min(128, K - c0)
-                    for j in range(max(1, width // gg)):
-                        pairs = prep[off:off + 512].view(np.uint16).reshape(128, 2)
-                        for m in (0, 15, 16, 31, 77, 127):
-                            row = _tm_row(b, m, f, which == B.GATE_UP)
-                            assert pairs[m, 0] == w[sn][e, row, c0 // gg + j]
-                            assert pairs[m, 1] == w[zn][e, row, c0 // gg + j]
-                        off += 512
-                    nch = width // 32
-                    words = prep[off:off + 64 * width].view(np.uint32).reshape(4, nch, 32, 4)
-                    for qq, c, lane in ((0, 0, 0), (1, nch - 1, 17), (3, 1, 31), (2, nch // 2, 9)):
-                        row = _tm_row(b, 32 * qq + lane, f, which == B.GATE_UP)
-                        for jw in range(4):
-                            wd = int(words[qq, c, lane, jw])
-                            for n in range(8):
-                                col = c0 + 32 * c + 8 * jw + order[n]
-                                assert (wd >> (4 * n)) & 15 == codes[e, row, col]
-                    off += 64 * width
-        assert off == prep.nbytes
 
 
 def test_prepare_rejects_out_of_range_scale_and_zero():

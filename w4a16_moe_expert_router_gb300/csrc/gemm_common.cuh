@@ -1,7 +1,6 @@
-// gemm_common.cuh -- device helpers shared by the two expert-GEMM kernels (the
-// tensor-memory kernel of gemm_tc.cu and the warp-MMA kernel of gemm_mma.cu):
-// the work list of (projection, expert, 128-row block, token chunk) items, the
-// launch arguments, bounded waits, and the 2-D TMA load of token rows.
+// gemm_common.cuh -- device helpers of the expert GEMM launch: the work list of
+// (projection, expert, 128-row block, token chunk) items, the launch arguments,
+// bounded waits, and the 2-D TMA load of token rows.
 #pragma once
 
 #include <cuda.h>
@@ -158,22 +157,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t
     }
     if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
   }
-}
-
-// Bounded wait by one thread (the others of its warp are not involved).
-__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, int32_t* err, volatile int* abort,
-                                            uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait_sleep(bar, parity, kSuspendNs)) {
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > limit_ns) {
-      atomicExch(err, kStatusTimeout);
-      *abort = 1;
-      return false;
-    }
-  }
-  return true;
 }
 
 // Bounded wait by one thread until a device-scope counter written by other CTAs

@@ -773,7 +773,7 @@ cudaError_t init_gemm_kernels() {
     err = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (err != cudaSuccess) return err;
   }
-  return init_gemm_tc_kernels();
+  return cudaSuccess;
 }
 
 cudaError_t launch_wait_selftest(int32_t* err, const int32_t* flag, uint64_t limit_ns, cudaStream_t st) {
@@ -794,9 +794,8 @@ cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, cons
   const int P = static_cast<int>(s.pairs());
   CUtensorMap map_x, map_h;
   if (!make_row_map(&map_x, ws.xs, P, s.d) || !make_row_map(&map_h, ws.h, P, s.f)) return cudaErrorInvalidValue;
-  // the per-weight order runs on the tensor-memory kernel; the group-factorised order here
-  if (s.red == 0) return launch_expert_gemm_tc(a, map_x, map_h, s.fmt == 1, num_sms, st);
-  auto* kern = s.fmt == 1 ? expert_gemm_mma_kernel<true, true> : expert_gemm_mma_kernel<true, false>;
+  auto* kern = s.fmt == 1 ? (s.red ? expert_gemm_mma_kernel<true, true> : expert_gemm_mma_kernel<false, true>)
+                          : (s.red ? expert_gemm_mma_kernel<true, false> : expert_gemm_mma_kernel<false, false>);
   return launch_pdl(kern, dim3(num_sms * kCtasPerSm), dim3(kThreads), kSmemBytes, st, a, map_x, map_h);
 }
 

@@ -109,14 +109,11 @@ cudaError_t launch_route(const Dims& s, const float* logits, int32_t* topk_idx, 
 // Sets the GEMM kernels' attributes on the current device.  Called once per
 // device before the first launch there.
 cudaError_t init_gemm_kernels();
-cudaError_t init_gemm_tc_kernels();
 
 // Expert GEMMs.  which is a mask: kGemmGateUp (x -> h, with the copy of the
 // token rows in expert order), kGemmDown (h -> y), or both in one launch (down
-// items wait for their expert's gate_up items).  Persistent grids sized from
-// the device's SM count.  The per-weight reduction order runs on the
-// tensor-memory kernel (gemm_tc.cu), the group-factorised order on the warp-MMA
-// kernel (gemm_mma.cu).
+// items wait for their expert's gate_up items).  A persistent grid sized from
+// the device's SM count.
 constexpr int kGemmGateUp = 1, kGemmDown = 2;
 cudaError_t launch_expert_gemm(int which, const Dims& s, const uint16_t* x, const int32_t* expert_offsets,
                                const int32_t* pair_list, const uint8_t* w_gate_up, const uint8_t* w_down,
@@ -131,11 +128,6 @@ cudaError_t launch_gather_rows(const Dims& s, const uint16_t* x, const int32_t* 
 // 32 rows, 128-byte swizzle.
 bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols);
 
-namespace gemm {
-struct Args;
-}
-cudaError_t launch_expert_gemm_tc(const gemm::Args& a, const CUtensorMap& map_x, const CUtensorMap& map_h, bool affine,
-                                  int num_sms, cudaStream_t st);
 
 cudaError_t launch_combine(const Dims& s, const float* topk_w, const float* y, const float* gamma, float eps,
                            uint16_t* out, cudaStream_t st);

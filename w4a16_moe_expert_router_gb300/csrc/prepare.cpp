@@ -6,25 +6,9 @@
 // library reads byte b of a row as column 2b (low nibble) and column 2b+1 (high
 // nibble); one fp16 scale and one fp16 zero-point per group of g columns.
 //
-// Two prepared streams, one per kernel, chosen by the shape's reduction field.
-//
-// Reduction 0 (the tensor-memory kernel, gemm_tc.cu).  Per expert, per block of
-// 128 GEMM rows, per stage of 128 columns (the last stage has 64 when K is an
-// odd multiple of 64):
-//   [(scale, second) pairs of the stage's groups: [group][row m], 4 bytes each]
-//   [codes: [quarter q][chunk c][lane l][4 words], 16 bytes per (q, c, l)]
-// with 128 / g groups (64 / g for a 64-column stage; one for g = 128) and chunks
-// c of 32 columns.  GEMM row m = 32 q + l; for gate_up (R = 2f) it is gate row
-// 64b + 16q + l for l < 16 and up row f + 64b + 16q + l - 16 for l >= 16 (a
-// gate row and its up row sit 16 lanes apart in one warp); for down (R = d) it
-// is row 128b + m.  Word j of (q, c, l) holds row m's columns c0 + 32c + 8j +
-// (0..7): nibble i (bits 4i..4i+3) is column offset 0, 2, 4, 6, 1, 3, 5, 7 for
-// i = 0..7.
-//
-// Reduction 1 (the warp-MMA kernel of the group-factorised order, gemm_mma.cu).
-// Per expert, per block of 128 GEMM rows, per stage of 128 columns (the last
-// stage has 64 when K is an odd multiple of 64), per warp strip w = 0..7 of 16
-// GEMM rows:
+// Prepared stream of one projection (rows R, contraction K, group g), per
+// expert, per block of 128 GEMM rows, per stage of 128 columns (the last stage
+// has 64 when K is an odd multiple of 64), per warp strip w = 0..7 of 16 GEMM rows:
 //   [(scale, zero) pairs of the strip for the ng groups in this stage, 64 ng bytes]
 //   [codes, 8 bytes per 16 columns per lane]
 // GEMM row r of strip w of block b is, for gate_up (R = 2f), gate row
@@ -52,7 +36,6 @@ struct Proj {
   int64_t E, R, K, g, nblocks;
   bool gate_up;
   int64_t f;  // gate_up: the gate/up split
-  int layout;  // the shape's reduction order: 0 tensor-memory stream, 1 warp-strip stream
 };
 
 bool proj_of(const moe_w4a16_shape* sh, int32_t which, Proj* p) {
@@ -60,11 +43,9 @@ bool proj_of(const moe_w4a16_shape* sh, int32_t which, Proj* p) {
   const size_t need = moe_w4a16_workspace_bytes(sh);
   if (need == 0) return false;  // invalid shape
   if (which == MOE_W4A16_GATE_UP) {
-    *p = Proj{sh->experts, 2 * int64_t(sh->inter), sh->hidden, sh->group_gate_up, sh->inter / 64, true, sh->inter,
-              sh->reduction};
+    *p = Proj{sh->experts, 2 * int64_t(sh->inter), sh->hidden, sh->group_gate_up, sh->inter / 64, true, sh->inter};
   } else if (which == MOE_W4A16_DOWN) {
-    *p = Proj{sh->experts, sh->hidden, sh->inter, sh->group_down, sh->hidden / moe::kBlockRows, false, sh->inter,
-              sh->reduction};
+    *p = Proj{sh->experts, sh->hidden, sh->inter, sh->group_down, sh->hidden / moe::kBlockRows, false, sh->inter};
   } else {
     return false;
   }
@@ -88,77 +69,8 @@ double half_value(uint16_t h) {
   return (h & 0x8000) ? -v : v;
 }
 
-// Matrix row of GEMM row m (0..127) of block b in the tensor-memory stream.
-inline int64_t tm_row(const Proj& p, int64_t b, int m) {
-  if (!p.gate_up) return moe::kBlockRows * b + m;
-  const int q = m / 32, l = m % 32;
-  return l < 16 ? 64 * b + 16 * q + l : p.f + 64 * b + 16 * q + (l - 16);
-}
-
-// Copies one (scale, second) pair or one code between the canonical arrays and the stream.
-template <bool kPack>
-inline void move_pair(uint16_t* sp, uint16_t* zp, uint8_t* out) {
-  if (kPack) {
-    std::memcpy(out, sp, 2);
-    std::memcpy(out + 2, zp, 2);
-  } else {
-    std::memcpy(sp, out, 2);
-    std::memcpy(zp, out + 2, 2);
-  }
-}
-template <bool kPack>
-inline void move_code(uint8_t* qrow, int64_t col, uint32_t& word, int nib) {
-  uint8_t* byte = qrow + (col >> 1);
-  const int sh = (col & 1) ? 4 : 0;
-  if (kPack) {
-    word |= uint32_t((*byte >> sh) & 15u) << (4 * nib);
-  } else {
-    const uint8_t code = uint8_t((word >> (4 * nib)) & 15u);
-    *byte = uint8_t((*byte & ~(15u << sh)) | (code << sh));
-  }
-}
-
-template <bool kPack>
-moe_w4a16_status walk_tm(const Proj& p, uint8_t* q, uint16_t* scale, uint16_t* zero, uint8_t* stream) {
-  static const int kColOfNibble[8] = {0, 2, 4, 6, 1, 3, 5, 7};
-  const int64_t rowb = p.K / 2, ng = p.K / p.g;
-  uint8_t* out = stream;
-  for (int64_t e = 0; e < p.E; ++e) {
-    uint8_t* qe = q + e * p.R * rowb;
-    uint16_t* se = scale + e * p.R * ng;
-    uint16_t* ze = zero + e * p.R * ng;
-    for (int64_t b = 0; b < p.nblocks; ++b) {
-      for (int64_t c0 = 0; c0 < p.K; c0 += 128) {
-        const int64_t width = std::min<int64_t>(128, p.K - c0);   // 128, or 64 for the last stage
-        const int ngs = int(std::max<int64_t>(1, width / p.g));  // groups in the stage (g divides K)
-        for (int j = 0; j < ngs; ++j) {
-          const int64_t grp = c0 / p.g + j;
-          for (int m = 0; m < moe::kBlockRows; ++m, out += 4) {
-            const int64_t row = tm_row(p, b, m);
-            move_pair<kPack>(se + row * ng + grp, ze + row * ng + grp, out);
-          }
-        }
-        for (int qq = 0; qq < 4; ++qq)
-          for (int c = 0; c < int(width / 32); ++c)
-            for (int l = 0; l < 32; ++l) {
-              const int64_t row = tm_row(p, b, 32 * qq + l);
-              for (int jw = 0; jw < 4; ++jw, out += 4) {
-                uint32_t word = 0;
-                if (!kPack) std::memcpy(&word, out, 4);
-                for (int i = 0; i < 8; ++i)
-                  move_code<kPack>(qe + row * rowb, c0 + 32 * c + 8 * jw + kColOfNibble[i], word, i);
-                if (kPack) std::memcpy(out, &word, 4);
-              }
-            }
-      }
-    }
-  }
-  return MOE_W4A16_OK;
-}
-
 template <bool kPack>
 moe_w4a16_status walk(const Proj& p, uint8_t* q, uint16_t* scale, uint16_t* zero, uint8_t* stream) {
-  if (p.layout == 0) return walk_tm<kPack>(p, q, scale, zero, stream);
   const int64_t rowb = p.K / 2, ng = p.K / p.g;
   uint8_t* out = stream;
   for (int64_t e = 0; e < p.E; ++e) {
