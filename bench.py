@@ -35,7 +35,7 @@ if ROOT not in sys.path:
 METRIC = "MoE expert-layer tokens/s at 256-token canvas; achieved HBM GB/s vs GB300 peak"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "expert_gemm_canvas256.txt")
-DOMINANT_SRC = os.path.join(ROOT, "w4a16_moe_expert_router_gb300", "csrc", "gemm_mma.cu")
+DOMINANT_SRC = [os.path.join(ROOT, "w4a16_moe_expert_router_gb300", "csrc", n) for n in ("gemm_mma.cu", "gemm_common.cuh")]
 
 
 def log(*a):
@@ -54,6 +54,8 @@ def parse_args(argv=None):
                    help="weight format: 0 asymmetric zero-point, 1 affine bias, 2 symmetric")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=2000)
+    p.add_argument("--graph", action="store_true",
+                   help="replay each step from a CUDA graph captured once (per weight copy) instead of launching it")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--sampler", action="store_true", help="time the per-step sampler instead of the layer")
     return p.parse_args(argv)
@@ -102,9 +104,13 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_hash(path: str) -> str:
-    with open(path, "rb") as fh:
-        return hashlib.sha256(fh.read()).hexdigest()[:16]
+def source_hash(paths) -> str:
+    """First 16 hex digits of the SHA-256 of the files' bytes, concatenated in order."""
+    h = hashlib.sha256()
+    for path in ([paths] if isinstance(paths, str) else paths):
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def profiled_traffic():
@@ -206,8 +212,9 @@ def run_ours(args, rank, world, local):
     seed = rank  # every rank denoises its own canvas
     x_bits = synth.make_x(wl, seed)
     logits = [synth.make_logits(wl, seed, layer=l) for l in range(layers)]
-    # two copies of every layer's weights alternate between steps (each > L2 already)
-    copies = 2 if layers == 1 else 1
+    # four copies of every layer's weights rotate between steps, so every step reads cold weights
+    # (one layer's weights already exceed L2; a 30-layer stack reads 30 distinct layers per step)
+    copies = 4 if layers == 1 else 1
     weights, gammas, touched = [], [], []
     for l in range(layers):
         w = synth.make_weights(wl, 0, layer=l)
@@ -216,7 +223,9 @@ def run_ours(args, rank, world, local):
             weights.append(runtime.PreparedWeights(torch.from_numpy(gu).to(dev), torch.from_numpy(dn).to(dev)))
         gammas.append(runtime.to_device_f32(synth.make_gamma(wl, 0, layer=l), dev) if wl.rmsnorm else None)
         del w, gu, dn
-    stream = torch.cuda.current_stream(dev)
+    # a dedicated stream (a CUDA graph cannot capture the legacy default stream)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
     sptr = stream.cuda_stream
     buf = runtime.alloc_buffers(wl, device=dev, stream=stream)
     x = runtime.to_device_x(x_bits, dev)
@@ -272,15 +281,33 @@ def run_ours(args, rank, world, local):
         step(i)
     torch.cuda.synchronize(dev)
 
+    graphs = []
+    if args.graph:
+        # one graph per weight copy: the whole step (every layer's route, experts, combine)
+        for c in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(c)
+            graphs.append(g)
+        for i in range(args.warmup):
+            graphs[i % copies].replay()
+        torch.cuda.synchronize(dev)
+
     K = args.steps
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(layers)] for _ in range(K)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)] if args.graph else None
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize(dev)
         t_start.record(stream)
         for i in range(K):
-            step(i, evs[i])
+            if args.graph:
+                sev[i][0].record(stream)
+                graphs[i % copies].replay()
+                sev[i][1].record(stream)
+            else:
+                step(i, evs[i])
         t_end.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
@@ -288,15 +315,25 @@ def run_ours(args, rank, world, local):
     if B.moe_w4a16_read_error(buf.workspace, stream) != B.OK:
         raise RuntimeError("a device-side wait timed out during the timed region")
     max_ms = max_over_ranks(elapsed_ms, world, dev)
+    if args.graph:
+        step_ms = np.array([e[0].elapsed_time(e[1]) for e in sev])
+        # the per-call attribution comes from eager steps run after the timed region
+        KA = min(K, 200)
+        for i in range(KA):
+            step(i, evs[i])
+        torch.cuda.synchronize(dev)
+    else:
+        KA = K
+        step_ms = np.array([evs[i][0][0].elapsed_time(evs[i][layers - 1][3]) for i in range(K)])
 
-    # per-kernel averages over the timed region
+    # per-call averages (route, experts, combine)
     parts = np.zeros((layers, 3))
-    for i in range(K):
+    for i in range(KA):
         for l in range(layers):
             e = evs[i][l]
             for j in range(3):
                 parts[l, j] += e[j].elapsed_time(e[j + 1])
-    parts /= K
+    parts /= KA
     route_us, experts_us, comb_us = (parts.mean(0) * 1e3).tolist()
 
     tokens_total = wl.tokens * K * world
@@ -350,6 +387,8 @@ def run_ours(args, rank, world, local):
         "steps": K,
         "warmup": args.warmup,
         "ms_per_step": ms_per_step,
+        "ms_per_step_median": float(np.median(step_ms)),
+        "ms_per_step_min": float(step_ms.min()),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -362,7 +401,8 @@ def run_ours(args, rank, world, local):
             "reduction": wl.reduction, "weight_format": wl.format,
             "experts_touched_per_layer": touched,
             "l2": f"inputs larger than L2: {layer_bytes / layers / 1e6:.0f} MB of expert weights per layer "
-                  f"vs 129 MB L2" + ("; two weight copies alternate between steps" if copies == 2 else ""),
+                  f"vs 129 MB L2" + (f"; {copies} weight copies rotate between steps" if copies > 1 else ""),
+            "launch": "CUDA graph replay of the whole step" if args.graph else "eager C-ABI calls",
             "parallelism": f"replicas x{world} (one canvas per GPU)",
         },
         "hbm_gbs": layer_gbs,
@@ -385,6 +425,7 @@ def run_ours(args, rank, world, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl)
+        result["cpu_baseline_1core"] = cpu_baseline(wl, nthreads=1)
     return result
 
 
@@ -417,31 +458,38 @@ class OracleCase:
         return time.perf_counter() - t0
 
 
-def cpu_baseline(wl):
-    nth = os.cpu_count() or 1
-    secs = OracleCase(wl).time_tokens(range(wl.tokens), nth)
+def cpu_baseline(wl, nthreads=None):
+    """The oracle on the host cores: all of them on one full layer of the canvas, or one
+    core on a sample of its tokens (scaled to the canvas)."""
+    nth = nthreads or os.cpu_count() or 1
     per_step = wl.layers  # one canvas through the whole stack
+    # the whole canvas either way: the oracle dequantises each touched expert once per call, so a
+    # sample of a few tokens would cost far more per token than the canvas does
+    secs = OracleCase(wl).time_tokens(range(wl.tokens), nth)
+    what = (f"one full {wl.name} layer ({wl.tokens} tokens: routing, fp64 dequantised expert FFNs, combine), "
+            f"{nth} thread" + ("s" if nth > 1 else ""))
     return {"value": wl.tokens / (secs * per_step), "unit": "tokens/s", "cores": nth, "kind": "oracle",
-            "sample": f"one full {wl.name} layer ({wl.tokens} tokens: routing, fp64 dequantised expert FFNs, "
-                      f"combine), {nth} threads" + (f"; scaled by {per_step} layers per step" if per_step > 1 else "")}
+            "sample": what + (f"; scaled by {per_step} layers per step" if per_step > 1 else "")}
 
 
 def run_reference(args, rank, world):
-    """The oracle as it stands, one token of the canvas per step, on the host cores."""
+    """The oracle as it stands on the host cores, the unit of cpu_baseline: each step one
+    full layer of the canvas (every token routed, its experts dequantised in fp64, the
+    combine), scaled by the layers of a stack; at most one warm-up step and a 120 s budget."""
     if rank != 0:
         return None
     wl = workload_of(args)
     nth = os.cpu_count() or 1
     case = OracleCase(wl)
-    for i in range(args.warmup):
-        case.time_tokens([i % wl.tokens], nth)
+    for i in range(min(args.warmup, 1)):
+        case.time_tokens(range(wl.tokens), nth)
     budget_s, t0, done, spent = 120.0, time.perf_counter(), 0, 0.0
     for i in range(args.steps):
-        spent += case.time_tokens([i % wl.tokens], nth) * wl.layers
+        spent += case.time_tokens(range(wl.tokens), nth) * wl.layers
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
-    value = done / spent
+    value = done * wl.tokens / spent
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": done,
         "warmup": args.warmup, "ms_per_step": 1e3 * spent / done, "higher_is_better": True, "scaling": "weak",
@@ -449,8 +497,9 @@ def run_reference(args, rank, world):
         "config": {"workload": wl.name, "tokens": wl.tokens, "hidden": wl.hidden, "inter": wl.inter,
                    "experts": wl.experts, "top_k": wl.top_k, "layers": wl.layers},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nth, "kind": "oracle",
-                         "sample": "one token of the canvas per step (its routing, its k experts dequantised "
-                                   f"in fp64, the combine), {nth} threads"
+                         "sample": f"one full {wl.name} layer of {wl.tokens} tokens per step (routing, fp64 "
+                                   f"dequantised expert FFNs, combine), {nth} threads"
+                                   + (f"; scaled by {wl.layers} layers per step" if wl.layers > 1 else "")
                                    + (f"; stopped after {done} of {args.steps} steps at the {budget_s:.0f} s budget"
                                       if done < args.steps else "")},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
