@@ -74,6 +74,7 @@ def lib():
                                              dbl, vp, ctypes.c_int, ctypes.c_int, vp]
             L.oracle_moe_forward_dense.argtypes = [ctypes.POINTER(_Shape), vp, vp, vp,
                                                    ctypes.POINTER(_Weights), vp]
+            L.oracle_block_front.argtypes = [i32, i32, i32, vp, vp, ctypes.c_float, vp, vp, vp]
             L.oracle_philox4x32_10.argtypes = [vp, vp, vp]
             L.oracle_log_f32.argtypes = [ctypes.c_float]
             L.oracle_log_f32.restype = ctypes.c_float
@@ -213,6 +214,23 @@ def forward_dense(x_bits: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, 
     if st != OK:
         raise ValueError(f"oracle_moe_forward_dense status {st}")
     return out
+
+
+def block_front(x_bits: np.ndarray, gamma: np.ndarray, eps: float, wr_bits: np.ndarray):
+    """The MoE block's pre-norm and router projection in their fixed fp32 order:
+    returns u (fp16 bit patterns [T][d]) and the router logits (fp32 [T][E])."""
+    x = _c(x_bits, np.uint16)
+    g = _c(gamma, np.float32)
+    w = _c(wr_bits, np.uint16)
+    T, d = x.shape
+    E = w.shape[0]
+    u = np.zeros((T, d), np.uint16)
+    logits = np.zeros((T, E), np.float32)
+    st = lib().oracle_block_front(int(T), int(d), int(E), _ptr(x), _ptr(g), float(eps), _ptr(w), _ptr(u),
+                                  _ptr(logits))
+    if st != OK:
+        raise ValueError(f"oracle_block_front status {st}")
+    return u, logits
 
 
 # ------------------------------------------------------------------ sampler

@@ -29,7 +29,9 @@
  *   - fused gate_up_proj: rows [0, f) are the gate projection, rows [f, 2f) the
  *     up projection; h = act(gate) * up;
  *   - act: GELU, tanh form by default, erf form selectable;
- *   - optional per-layer RMSNorm of the combined output: gamma * u / sqrt(mean(u^2) + eps).
+ *   - optional per-layer RMSNorm of the combined output: gamma * u / sqrt(mean(u^2) + eps);
+ *   - the MoE block around the layer (pre-norm, router projection, residual): see
+ *     oracle_block_front below.
  *
  * Everything below is the plain definition: weights are dequantised into a dense
  * fp64 matrix, the FFN is two fp64 matrix-vector products, and the combine is a
@@ -409,4 +411,82 @@ int oracle_moe_forward_dense(const oracle_shape* s, const uint16_t* x, const int
 done:
   free(Wgu); free(Wd); free(G); free(xd); free(a); free(h); free(y);
   return status;
+}
+
+/* ------------------------------------------------------------- MoE block ---- */
+
+/* The block around the expert layer.  [MC] "the kernels we built": RMSNorm in one
+ * launch (180 of them per forward); "what the model is": a router sends each token
+ * to its top-8 of 128 experts.  The pages print no formula for the block; the
+ * reading taken here (listed in the design notes) is the pre-norm residual block
+ *   block(x) = x + layer(u),  u = fp16(gamma * (x * r)),  r = 1 / sqrt(ss / d + eps),
+ *   ss = sum_k x_k^2,  logits[t][e] = sum_k u[t][k] * Wr[e][k]  (Wr fp16 [E][d]),
+ * with the layer's fp32 output added to x before the one rounding to fp16.
+ *
+ * The logits decide the routing, an integer result, so ss and the logits are
+ * defined in fp32 with one fixed order of operations, which the GPU reproduces
+ * bit for bit: the d columns are dealt to 32 lanes in 8-column chunks (lane l
+ * takes chunks l, l + 32, l + 64, ... in that order) and each lane accumulates
+ * fmaf(a_k, b_k, acc) column by column from acc = 0; the 32 lane sums are then
+ * combined by a butterfly: for off = 16, 8, 4, 2, 1 every lane l adds the sum of
+ * lane l ^ off, and all lanes end with the same value.  d must be a multiple of
+ * 256.  r, v = x_k * r and gamma_k * v are single fp32 operations (IEEE division
+ * and square root), u rounds to nearest even. */
+
+static float lane_butterfly_sum(float p[32]) {
+  for (int off = 16; off >= 1; off >>= 1) {
+    float q[32];
+    for (int l = 0; l < 32; ++l) q[l] = p[l] + p[l ^ off];
+    memcpy(p, q, sizeof(q));
+  }
+  return p[0];
+}
+
+static float dot_lanes(int64_t d, const float* a, const float* b) {
+  float p[32];
+  for (int l = 0; l < 32; ++l) {
+    float acc = 0.0f;
+    for (int64_t c = l; c < d / 8; c += 32)
+      for (int i = 0; i < 8; ++i) acc = fmaf(a[8 * c + i], b[8 * c + i], acc);
+    p[l] = acc;
+  }
+  return lane_butterfly_sum(p);
+}
+
+/* x fp16 bits [T][d], gamma fp32 [d], wr fp16 bits [E][d] -> u fp16 bits [T][d],
+ * logits fp32 [T][E].  Non-finite inputs give ORACLE_ERR_NONFINITE. */
+int oracle_block_front(int T, int d, int E, const uint16_t* x, const float* gamma, float eps, const uint16_t* wr,
+                       uint16_t* u_out, float* logits) {
+  if (T < 0 || d <= 0 || d % 256 != 0 || E < 1) return ORACLE_ERR_SHAPE;
+  float* xf = (float*)malloc(sizeof(float) * (size_t)d);
+  float* uf = (float*)malloc(sizeof(float) * (size_t)d);
+  float* wf = (float*)malloc(sizeof(float) * (size_t)E * (size_t)d);
+  if (!xf || !uf || !wf) {
+    free(xf);
+    free(uf);
+    free(wf);
+    return ORACLE_ERR_ALLOC;
+  }
+  int st = ORACLE_OK;
+  for (int64_t i = 0; i < (int64_t)E * d; ++i) wf[i] = (float)oracle_half_to_double(wr[i]);
+  for (int t = 0; t < T && st == ORACLE_OK; ++t) {
+    for (int k = 0; k < d; ++k) {
+      xf[k] = (float)oracle_half_to_double(x[(int64_t)t * d + k]);
+      if (!isfinite(xf[k]) || !isfinite(gamma[k])) st = ORACLE_ERR_NONFINITE;
+    }
+    const float ss = dot_lanes(d, xf, xf);
+    const float r = 1.0f / sqrtf(ss / (float)d + eps);
+    for (int k = 0; k < d; ++k) {
+      const float v = xf[k] * r;
+      const float w = gamma[k] * v;
+      const uint16_t h = oracle_double_to_half((double)w);
+      u_out[(int64_t)t * d + k] = h;
+      uf[k] = (float)oracle_half_to_double(h);
+    }
+    for (int e = 0; e < E; ++e) logits[(int64_t)t * E + e] = dot_lanes(d, uf, wf + (int64_t)e * d);
+  }
+  free(xf);
+  free(uf);
+  free(wf);
+  return st;
 }

@@ -352,3 +352,72 @@ def test_format_identities_through_the_layer():
     assert np.array_equal(run(w, 2), run(eight, 0))
     assert not np.array_equal(run(w, 2), run(w, 0))
     assert not np.array_equal(run(w, 1), run(w, 0))
+
+
+# ------------------------------------------------------------ MoE block
+# The block around the layer: pre-norm u = fp16(gamma * x / sqrt(mean(x^2) + eps)),
+# router logits = u . Wr (model card "srswti/axe-diffusion-ksl-xe", "the kernels we
+# built": one-launch RMSNorm; "what the model is": top-8 of 128 experts), computed
+# in fp32 in a fixed order so that the routing they decide is reproducible.
+
+def _block_inputs(T, d, E, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, d)).astype(np.float16).view(np.uint16)
+    gamma = (1.0 + 0.1 * rng.standard_normal(d)).astype(np.float32)
+    wr = (rng.standard_normal((E, d)) / np.sqrt(d)).astype(np.float16).view(np.uint16)
+    return x, gamma, wr
+
+
+def test_block_front_u_is_the_fp16_rmsnorm():
+    """u against the fp64 RMSNorm rounded to fp16: equal except where the fp32
+    evaluation lands on the other side of an fp16 rounding boundary (one ulp)."""
+    x, gamma, wr = _block_inputs(32, 512, 8, 1)
+    u, _ = oracle.block_front(x, gamma, 1e-6, wr)
+    xf = x.view(np.float16).astype(np.float64)
+    ref = (gamma * xf / np.sqrt((xf * xf).mean(1, keepdims=True) + 1e-6)).astype(np.float16)
+    got = u.view(np.float16)
+    assert (got == ref).mean() > 0.999
+    ulp = np.abs(np.spacing(ref.astype(np.float16))).astype(np.float64)
+    assert np.all(np.abs(got.astype(np.float64) - ref.astype(np.float64)) <= ulp)
+
+
+def test_block_front_logits_within_the_fp32_bound():
+    """logits against the fp64 dot product of the same u and Wr, inside the classical
+    bound for a sum of n fp32 terms: |err| <= n eps / (1 - n eps) * sum |u_k w_k|, with
+    n = d / 256 * 8 sequential terms per lane plus 5 butterfly levels."""
+    T, d, E = 16, 2048, 128
+    x, gamma, wr = _block_inputs(T, d, E, 2)
+    u, logits = oracle.block_front(x, gamma, 1e-6, wr)
+    uf = u.view(np.float16).astype(np.float64)
+    wf = wr.view(np.float16).astype(np.float64)
+    ref = uf @ wf.T
+    n = d // 256 * 8 + 5
+    eps = 2.0 ** -24
+    bound = n * eps / (1 - n * eps) * (np.abs(uf) @ np.abs(wf).T)
+    assert np.all(np.abs(logits.astype(np.float64) - ref) <= bound)
+    # a wrong row of Wr, a transposed operand or a dropped chunk is far outside the bound
+    assert np.abs(logits.astype(np.float64) - uf @ np.roll(wf, 1, axis=0).T).max() > 100 * bound.max()
+
+
+def test_block_front_one_hot_router_copies_u():
+    """A router whose row e is 1 at column c_e and 0 elsewhere gives logits[t][e] = u[t][c_e]
+    exactly (one exact product, the rest exact zeros)."""
+    T, d, E = 8, 256, 16
+    x, gamma, _ = _block_inputs(T, d, E, 3)
+    cols = np.array([0, 7, 8, 255, 31, 32, 100, 200, 63, 64, 1, 2, 250, 17, 128, 129])
+    wr = np.zeros((E, d), np.float16)
+    wr[np.arange(E), cols] = 1.0
+    u, logits = oracle.block_front(x, gamma, 1e-6, wr.view(np.uint16))
+    assert np.array_equal(logits, u.view(np.float16)[:, cols].astype(np.float32))
+
+
+def test_block_front_constant_rows_closed_form():
+    """x = 2 everywhere, gamma = 1, eps = 0: ss = 4 d exactly, r = 1/2, u = 1.0 exactly;
+    x = c with eps: u = fp16(c / sqrt(c^2 + eps)) for every column."""
+    d = 512
+    x = np.full((2, d), 2.0, np.float16).view(np.uint16)
+    u, _ = oracle.block_front(x, np.ones(d, np.float32), 0.0, np.zeros((1, d), np.uint16))
+    assert np.all(u == 0x3C00)
+    x = np.full((1, d), 0.5, np.float16).view(np.uint16)
+    u, _ = oracle.block_front(x, np.ones(d, np.float32), 1.0, np.zeros((1, d), np.uint16))
+    assert np.all(u.view(np.float16) == np.float16(0.5 / np.sqrt(1.25)))
