@@ -137,7 +137,8 @@ typedef struct {
  * activations h (fp16 [T*k][f]), the token rows copied in expert order
  * (fp16 [T*k][d]), per-pair expert outputs (fp32 [T*k][d]) and routing scratch
  * (per-CTA expert counts, per-pair ranks) plus a small header (error word, work
- * counters).  It must be initialised once with
+ * counters), plus, for moe_w4a16_block, the normalised input u (fp16 [T][d]) and
+ * the router logits (fp32 [T][E]).  It must be initialised once with
  * moe_w4a16_workspace_init before its first use; later calls leave it ready. */
 MOE_W4A16_API size_t moe_w4a16_workspace_bytes(const moe_w4a16_shape* shape);
 
@@ -202,6 +203,42 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_combine(const moe_w4a16_shape* shape, c
  * moe_w4a16_workspace_init. */
 MOE_W4A16_API moe_w4a16_status moe_w4a16_read_error(const void* workspace, size_t workspace_bytes, void* stream,
                                       moe_w4a16_status* device_status);
+
+/* ---- the MoE block around the layer ------------------------------------------
+ * A pre-norm residual block (model card "srswti/axe-diffusion-ksl-xe", "the
+ * kernels we built": the RMSNorm of a block in one launch; "what the model is":
+ * a router picks each token's top-8 of 128 experts):
+ *   u       = fp16(gamma * (x * r)),  r = 1 / sqrt(ss / d + eps),  ss = sum_k x_k^2
+ *   logits  = u . Wr^T                 (Wr fp16 [E][d], fp32 results [T][E])
+ *   out     = fp16(x + layer(u))       (layer: route + experts + combine, fp32 sum
+ *                                       with x before the one rounding)
+ * The logits decide the routing, so ss and the logits are defined in fp32 with
+ * one fixed order of operations and are reproducible bit for bit off the GPU:
+ * the d columns are dealt to 32 lanes in 8-column chunks (lane l takes chunks
+ * l, l + 32, ..., in that order), each lane accumulates fmaf(a_k, b_k, acc)
+ * column by column from 0, and the 32 lane sums meet in an xor butterfly
+ * (offsets 16, 8, 4, 2, 1); r, x_k * r and gamma_k * (x_k * r) are single IEEE
+ * fp32 operations and u rounds to nearest even.  d must be a multiple of 256
+ * (ERR_SHAPE otherwise); norm_eps >= 0 and finite (ERR_VALUE).
+ *
+ * moe_w4a16_block_front: the pre-norm and the router projection alone.
+ *   x         fp16 [T][d], read       norm_gamma  fp32 [d], read
+ *   router_w  fp16 [E][d], read       u  fp16 [T][d], written    logits  fp32 [T][E], written
+ * moe_w4a16_block: the whole block on `stream`: the front (u and the logits go to
+ * the workspace), moe_w4a16_route on the logits (routing is written as that call
+ * writes it), the experts on u and the combine with the residual.
+ *   out  fp16 [T][d], written; may be x itself (each element is read before it is
+ *        written by the same thread), must not overlap the workspace or routing.
+ * Weights, workspace and routing follow the rules of moe_w4a16_forward. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_block_front(const moe_w4a16_shape* shape, const uint16_t* x,
+                                                     const float* norm_gamma, float norm_eps,
+                                                     const uint16_t* router_w, uint16_t* u, float* logits,
+                                                     void* stream);
+MOE_W4A16_API moe_w4a16_status moe_w4a16_block(const moe_w4a16_shape* shape, const uint16_t* x,
+                                               const float* norm_gamma, float norm_eps, const uint16_t* router_w,
+                                               const moe_w4a16_routing* routing, const moe_w4a16_weights* weights,
+                                               uint16_t* out, void* workspace, size_t workspace_bytes,
+                                               void* stream);
 
 /* ---- per-step sampler ------------------------------------------------------
  * One denoising step's sampling over a canvas (model card

@@ -100,6 +100,32 @@ def test_pointer_and_workspace_validation_before_any_launch():
     assert L.moe_w4a16_route(ctypes.byref(sh), 4096, None, 4096, ws, None) == B.ERR_NULL
 
 
+def test_block_validation_before_any_launch():
+    """The MoE block's calls check shapes, pointers, alignment, workspace and eps on
+    the host; d must be a multiple of 256 (the lanes' 8-column chunks)."""
+    L = B.lib()
+    sh = _shape()                      # d = 256
+    ws = B.moe_w4a16_workspace_bytes(sh)
+    r = B.Routing(4096, 4096, 4096, 4096)
+    w = B.Weights(4096, 4096)
+    blk = lambda x, g, wr, out, wsb, eps=1e-6, sh=sh, rr=r, ww=w: L.moe_w4a16_block(
+        ctypes.byref(sh), x, g, eps, wr, ctypes.byref(rr), ctypes.byref(ww), out, 4096, wsb, None)
+    assert blk(None, 4096, 4096, 4096, ws) == B.ERR_NULL
+    assert blk(4096, None, 4096, 4096, ws) == B.ERR_NULL
+    assert blk(4096, 4096, 4096, 4096, ws, rr=B.Routing(4096, 4096, None, 4096)) == B.ERR_NULL
+    assert blk(4104, 4096, 4096, 4096, ws) == B.ERR_ALIGN
+    assert blk(4096, 4096, 4100, 4096, ws) == B.ERR_ALIGN
+    assert blk(4096, 4096, 4096, 4096, ws - 1) == B.ERR_WORKSPACE
+    assert blk(4096, 4096, 4096, 4096, ws, eps=-1.0) == B.ERR_VALUE
+    sh384 = _shape(hidden=384, group_gate_up=128)
+    assert blk(4096, 4096, 4096, 4096, 1 << 30, sh=sh384) == B.ERR_SHAPE
+    front = lambda x, g, wr, u, lg, sh=sh: L.moe_w4a16_block_front(ctypes.byref(sh), x, g, 1e-6, wr, u, lg, None)
+    assert front(4096, 4096, 4096, 4096, None) == B.ERR_NULL
+    assert front(4096, 4096, 4096, 4104, 4096) == B.ERR_ALIGN
+    assert front(4096, 4096, 4096, 4096, 4096, sh=sh384) == B.ERR_SHAPE
+    assert B.moe_w4a16_workspace_bytes(sh) >= 16 * 256 * 2 + 16 * 8 * 4  # room for u and the logits
+
+
 def test_zero_tokens_is_a_no_op():
     L = B.lib()
     sh = _shape(tokens=0)

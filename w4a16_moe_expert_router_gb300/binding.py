@@ -26,7 +26,8 @@ EXPORTED = ("moe_w4a16_workspace_bytes", "moe_w4a16_workspace_init", "moe_w4a16_
             "moe_w4a16_experts",
             "moe_w4a16_gate_up", "moe_w4a16_down", "moe_w4a16_combine", "moe_w4a16_read_error", "moe_w4a16_pack", "moe_w4a16_unpack", "moe_w4a16_prepared_bytes",
             "moe_w4a16_prepare", "moe_w4a16_unprepare", "moe_w4a16_status_string", "moe_w4a16_forward_noalloc",
-            "moe_w4a16_selftest_wait_timeout", "moe_w4a16_sampler_workspace_bytes", "moe_w4a16_sample")
+            "moe_w4a16_selftest_wait_timeout", "moe_w4a16_sampler_workspace_bytes", "moe_w4a16_sample",
+            "moe_w4a16_block_front", "moe_w4a16_block")
 
 NOALLOC_SCRATCH_BYTES = 40 << 20  # MOE_W4A16_NOALLOC_SCRATCH_BYTES
 
@@ -91,6 +92,11 @@ def lib() -> ctypes.CDLL:
             L.moe_w4a16_forward_noalloc.argtypes = [P(Shape), vp, P(Routing), P(Weights), vp, ctypes.c_float, vp,
                                                     vp]
             L.moe_w4a16_forward_noalloc.restype = st
+            L.moe_w4a16_block_front.argtypes = [P(Shape), vp, vp, ctypes.c_float, vp, vp, vp, vp]
+            L.moe_w4a16_block_front.restype = st
+            L.moe_w4a16_block.argtypes = [P(Shape), vp, vp, ctypes.c_float, vp, P(Routing), P(Weights), vp, vp, sz,
+                                          vp]
+            L.moe_w4a16_block.restype = st
             L.moe_w4a16_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint64, vp]
             L.moe_w4a16_selftest_wait_timeout.restype = st
             L.moe_w4a16_sampler_workspace_bytes.argtypes = [P(Sampler)]
@@ -192,6 +198,21 @@ def moe_w4a16_forward(shape: Shape, x, routing: RoutingBuffers, gate_up, down, n
     _check(lib().moe_w4a16_forward(ctypes.byref(shape), _dptr(x), ctypes.byref(r), ctypes.byref(w),
                                    _dptr(norm_gamma), float(norm_eps), _dptr(out), _dptr(workspace),
                                    _nbytes(workspace), _stream(stream)), "moe_w4a16_forward")
+
+
+def moe_w4a16_block_front(shape: Shape, x, norm_gamma, norm_eps: float, router_w, u, logits, stream=None) -> None:
+    _check(lib().moe_w4a16_block_front(ctypes.byref(shape), _dptr(x), _dptr(norm_gamma), float(norm_eps),
+                                       _dptr(router_w), _dptr(u), _dptr(logits), _stream(stream)),
+           "moe_w4a16_block_front")
+
+
+def moe_w4a16_block(shape: Shape, x, norm_gamma, norm_eps: float, router_w, routing: RoutingBuffers, gate_up, down,
+                    out, workspace, stream=None) -> None:
+    r = routing.c()
+    w = Weights(_dptr(gate_up), _dptr(down))
+    _check(lib().moe_w4a16_block(ctypes.byref(shape), _dptr(x), _dptr(norm_gamma), float(norm_eps), _dptr(router_w),
+                                 ctypes.byref(r), ctypes.byref(w), _dptr(out), _dptr(workspace), _nbytes(workspace),
+                                 _stream(stream)), "moe_w4a16_block")
 
 
 def moe_w4a16_forward_noalloc(shape: Shape, x, routing: RoutingBuffers, gate_up, down, norm_gamma,

@@ -67,7 +67,9 @@ moe_w4a16_status device_state(const DeviceState** out) {
       st.status = MOE_W4A16_ERR_DEVICE;
     } else {
       st.num_sms = sms;
-      st.status = moe::init_gemm_kernels() == cudaSuccess ? MOE_W4A16_OK : MOE_W4A16_ERR_CUDA;
+      st.status = (moe::init_gemm_kernels() == cudaSuccess && moe::init_block_kernels() == cudaSuccess)
+                      ? MOE_W4A16_OK
+                      : MOE_W4A16_ERR_CUDA;
     }
     st.ready = true;
   }
@@ -175,6 +177,7 @@ struct FwdArgs {
   size_t ws_bytes;
   void* stream;
   bool clear_header;  // clear the workspace header (error word, work counters) before the launches
+  const uint16_t* residual = nullptr;  // combine: out = fp16(residual + u) (the MoE block)
 };
 
 // Validates what the requested steps read and write, then launches them in order.
@@ -211,7 +214,8 @@ moe_w4a16_status run_forward_steps(const moe_w4a16_shape* shape, int steps, cons
                                       (steps & kGateUp) ? a.weights->gate_up : nullptr,
                                       (steps & kDown) ? a.weights->down : nullptr, ws, dev->num_sms, cs) != cudaSuccess)
     return MOE_W4A16_ERR_CUDA;
-  if ((steps & kCombine) && moe::launch_combine(s, r.topk_w, ws.y, a.gamma, a.eps, a.out, cs) != cudaSuccess)
+  if ((steps & kCombine) &&
+      moe::launch_combine(s, r.topk_w, ws.y, a.gamma, a.eps, a.residual, a.out, cs) != cudaSuccess)
     return MOE_W4A16_ERR_CUDA;
   return MOE_W4A16_OK;
 }
@@ -262,6 +266,58 @@ moe_w4a16_status moe_w4a16_combine(const moe_w4a16_shape* shape, const moe_w4a16
                                    size_t workspace_bytes, void* stream) {
   return run_forward_steps(shape, kCombine, FwdArgs{nullptr, routing, nullptr, norm_gamma, norm_eps, out, workspace,
                                                     workspace_bytes, stream, false});
+}
+
+moe_w4a16_status moe_w4a16_block_front(const moe_w4a16_shape* shape, const uint16_t* x, const float* norm_gamma,
+                                       float norm_eps, const uint16_t* router_w, uint16_t* u, float* logits,
+                                       void* stream) {
+  Dims s;
+  moe_w4a16_status st = check_shape(shape, &s);
+  if (st != MOE_W4A16_OK) return st;
+  if (s.d % 256 != 0) return MOE_W4A16_ERR_SHAPE;
+  if (s.T == 0) return MOE_W4A16_OK;
+  if (!x || !norm_gamma || !router_w || !u || !logits) return MOE_W4A16_ERR_NULL;
+  if (!aligned16(x) || !aligned16(norm_gamma) || !aligned16(router_w) || !aligned16(u) || !aligned16(logits))
+    return MOE_W4A16_ERR_ALIGN;
+  if (!(norm_eps >= 0.f) || !(norm_eps <= 3.4e38f)) return MOE_W4A16_ERR_VALUE;
+  const DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != MOE_W4A16_OK) return st;
+  return cuda_status(moe::launch_block_front(s, x, norm_gamma, norm_eps, router_w, u, logits,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+moe_w4a16_status moe_w4a16_block(const moe_w4a16_shape* shape, const uint16_t* x, const float* norm_gamma,
+                                 float norm_eps, const uint16_t* router_w, const moe_w4a16_routing* routing,
+                                 const moe_w4a16_weights* weights, uint16_t* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  Dims s;
+  moe_w4a16_status st = check_shape(shape, &s);
+  if (st != MOE_W4A16_OK) return st;
+  if (s.d % 256 != 0) return MOE_W4A16_ERR_SHAPE;
+  if (!routing || !weights) return MOE_W4A16_ERR_NULL;
+  if (s.T == 0) return MOE_W4A16_OK;
+  const moe_w4a16_routing& r = *routing;
+  if (!x || !norm_gamma || !router_w || !out || !workspace || !weights->gate_up || !weights->down || !r.topk_idx ||
+      !r.topk_w || !r.expert_offsets || !r.pair_list)
+    return MOE_W4A16_ERR_NULL;
+  if (!aligned16(x) || !aligned16(norm_gamma) || !aligned16(router_w) || !aligned16(out) || !aligned16(workspace) ||
+      !aligned16(weights->gate_up) || !aligned16(weights->down) || !aligned16(r.topk_idx) || !aligned16(r.topk_w) ||
+      !aligned16(r.expert_offsets) || !aligned16(r.pair_list))
+    return MOE_W4A16_ERR_ALIGN;
+  if (workspace_bytes < moe::ws_total(s)) return MOE_W4A16_ERR_WORKSPACE;
+  if (!(norm_eps >= 0.f) || !(norm_eps <= 3.4e38f)) return MOE_W4A16_ERR_VALUE;
+  const DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != MOE_W4A16_OK) return st;
+  auto* base = static_cast<uint8_t*>(workspace);
+  auto* u = reinterpret_cast<uint16_t*>(base + moe::ws_u_offset(s));
+  auto* logits = reinterpret_cast<float*>(base + moe::ws_logits_offset(s));
+  const auto cs = static_cast<cudaStream_t>(stream);
+  if (moe::launch_block_front(s, x, norm_gamma, norm_eps, router_w, u, logits, cs) != cudaSuccess ||
+      moe::launch_route(s, logits, r.topk_idx, r.topk_w, r.expert_offsets, r.pair_list, workspace, cs) != cudaSuccess)
+    return MOE_W4A16_ERR_CUDA;
+  FwdArgs fa{u, routing, weights, nullptr, 0.f, out, workspace, workspace_bytes, stream, false};
+  fa.residual = x;
+  return run_forward_steps(shape, kGateUp | kDown | kCombine, fa);
 }
 
 moe_w4a16_status moe_w4a16_read_error(const void* workspace, size_t workspace_bytes, void* stream,

@@ -98,10 +98,12 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restri
 }
 
 // Without RMSNorm: one 128-thread CTA per quarter of a token row (d / 4 columns,
-// one float4 per thread and row), the same arithmetic in the same order.
+// one float4 per thread and row), the same arithmetic in the same order; with a
+// residual x, out = fp16(x + u) (one fp32 addition after the rank-order sum).
 __global__ void __launch_bounds__(128) combine_quarter_kernel(const float* __restrict__ topk_w,
                                                              const float* __restrict__ y, int d, int k,
-                                                             uint16_t* __restrict__ out) {
+                                                             const uint16_t* residual,  // may equal out
+                                                             uint16_t* out) {
   grid_dependents_launch();
   grid_dependency_wait();
   const int t = blockIdx.x >> 2, q = blockIdx.x & 3;
@@ -126,6 +128,12 @@ __global__ void __launch_bounds__(128) combine_quarter_kernel(const float* __res
         acc.z = fmaf(wr[r], v[r].z, acc.z);
         acc.w = fmaf(wr[r], v[r].w, acc.w);
       }
+    if (residual) {
+      const uint2 xr = reinterpret_cast<const uint2*>(residual + static_cast<size_t>(t) * d)[i4];
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&xr.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&xr.y));
+      acc = make_float4(__fadd_rn(a.x, acc.x), __fadd_rn(a.y, acc.y), __fadd_rn(b.x, acc.z), __fadd_rn(b.y, acc.w));
+    }
     const __half2 lo = __floats2half2_rn(acc.x, acc.y);
     const __half2 hi = __floats2half2_rn(acc.z, acc.w);
     o2[i4] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
@@ -135,9 +143,10 @@ __global__ void __launch_bounds__(128) combine_quarter_kernel(const float* __res
 }  // namespace
 
 cudaError_t launch_combine(const Dims& s, const float* topk_w, const float* y, const float* gamma, float eps,
-                           uint16_t* out, cudaStream_t st) {
+                           const uint16_t* residual, uint16_t* out, cudaStream_t st) {
+  if (gamma && residual) return cudaErrorInvalidValue;
   if (gamma) return launch_pdl(combine_kernel<true>, dim3(s.T), dim3(kThreads), 0, st, topk_w, y, s.d, s.k, gamma, eps, out);
-  return launch_pdl(combine_quarter_kernel, dim3(4 * s.T), dim3(128), 0, st, topk_w, y, s.d, s.k, out);
+  return launch_pdl(combine_quarter_kernel, dim3(4 * s.T), dim3(128), 0, st, topk_w, y, s.d, s.k, residual, out);
 }
 
 }  // namespace moe

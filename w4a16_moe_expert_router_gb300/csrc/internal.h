@@ -21,6 +21,7 @@ constexpr int kBoxCols = 64;      // contraction columns per TMA box of token ro
 constexpr int kRowBoxRows = 32;   // token rows per TMA box
 constexpr int kChunkN = 32;       // tokens (pairs) per work item
 constexpr int kMaxExperts = 256;
+constexpr int kMaxHidden = 8192;
 constexpr int kMaxTopK = 8;
 constexpr int64_t kMaxPairs = int64_t(1) << 22;
 
@@ -64,7 +65,11 @@ inline size_t ws_y_bytes(const Dims& s) { return size_t(s.pairs()) * s.d * 4; }
 inline size_t ws_route_offset(const Dims& s) { return (ws_y_offset(s) + ws_y_bytes(s) + 255) / 256 * 256; }
 inline size_t ws_route_hist_bytes(const Dims& s) { return size_t((s.T + 7) / 8) * s.E * 4; }
 inline size_t ws_route_bytes(const Dims& s) { return ws_route_hist_bytes(s) + size_t(s.pairs()) * 4; }
-inline size_t ws_total(const Dims& s) { return ws_route_offset(s) + ws_route_bytes(s); }
+// the MoE block's normalised input u (fp16 [T][d]) and router logits (fp32 [T][E])
+inline size_t ws_u_offset(const Dims& s) { return (ws_route_offset(s) + ws_route_bytes(s) + 255) / 256 * 256; }
+inline size_t ws_u_bytes(const Dims& s) { return size_t(s.T) * s.d * 2; }
+inline size_t ws_logits_offset(const Dims& s) { return (ws_u_offset(s) + ws_u_bytes(s) + 255) / 256 * 256; }
+inline size_t ws_total(const Dims& s) { return ws_logits_offset(s) + size_t(s.T) * s.E * 4; }
 
 // Device pointers of one workspace's parts.
 struct GemmWorkspace {
@@ -129,8 +134,15 @@ cudaError_t launch_gather_rows(const Dims& s, const uint16_t* x, const int32_t* 
 bool make_row_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols);
 
 
+// Combine (and optional RMSNorm, or optional residual add out = fp16(x + u); not both).
 cudaError_t launch_combine(const Dims& s, const float* topk_w, const float* y, const float* gamma, float eps,
-                           uint16_t* out, cudaStream_t st);
+                           const uint16_t* residual, uint16_t* out, cudaStream_t st);
+
+// The MoE block's pre-norm and router projection (block.cu): u fp16 [T][d] and the
+// router logits fp32 [T][E] from the residual stream x.  d a multiple of 256.
+cudaError_t init_block_kernels();
+cudaError_t launch_block_front(const Dims& s, const uint16_t* x, const float* gamma, float eps, const uint16_t* wr,
+                               uint16_t* u, float* logits, cudaStream_t st);
 
 // Per-step sampler (sampler.cu): one streaming pass over the logits (grid of
 // vocabulary splits x positions) writing 32-byte partials to the workspace, then

@@ -77,6 +77,20 @@ def run_layer(buf: Buffers, x: torch.Tensor, logits: torch.Tensor, w: PreparedWe
     return o
 
 
+def run_block(buf: Buffers, x: torch.Tensor, gamma_pre: torch.Tensor, router_w: torch.Tensor, w: PreparedWeights,
+              eps: float = 1e-6, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The MoE block: pre-norm, router projection, routing, experts, combine plus the residual."""
+    o = buf.out if out is None else out
+    B.moe_w4a16_block(buf.shape, x, gamma_pre, eps, router_w, buf.routing, w.gate_up, w.down, o, buf.workspace,
+                      stream)
+    return o
+
+
+def to_device_u16(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """fp16 bit patterns (uint16) as an fp16 device tensor."""
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).to(device)
+
+
 def to_device_x(x_bits: np.ndarray, device="cuda") -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(x_bits).view(np.float16)).to(device)
 

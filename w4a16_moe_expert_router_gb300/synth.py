@@ -20,7 +20,8 @@ library's choice for the synthetic layer.
 
 Distributions: packed weight bytes uniform over 0..255 (two independent uniform
 nibbles); scale fp16(U(0.005, 0.02)); zero-point fp16(U(6, 9)); x fp16(N(0,1));
-router logits fp32 N(0,1).  Every tensor draws from its own stream, derived from
+router logits fp32 N(0,1); for the MoE block around the layer, router weights
+fp16(N(0, 1/d)) and a pre-norm weight N(1, 0.1).  Every tensor draws from its own stream, derived from
 (seed, layer, tensor number) in a fixed order, so any tensor can be regenerated
 alone.
 """
@@ -63,7 +64,7 @@ WORKLOADS = {
 }
 
 # tensor numbers of the derived streams (fixed order)
-_X, _LOGITS, _GUQ, _GUS, _GUZ, _DQ, _DS, _DZ, _GAMMA = range(9)
+_X, _LOGITS, _GUQ, _GUS, _GUZ, _DQ, _DS, _DZ, _GAMMA, _ROUTER, _GAMMA_PRE = range(11)
 
 
 def _rng(seed: int, layer: int, tensor: int) -> np.random.Generator:
@@ -122,3 +123,15 @@ def _second(w: Workload, z: np.ndarray, scale_bits: np.ndarray) -> np.ndarray:
 def make_gamma(w: Workload, seed: int = 0, layer: int = 0) -> np.ndarray:
     """RMSNorm weight fp32 [d] ~ N(1, 0.1)."""
     return np.ascontiguousarray(1.0 + 0.1 * _rng(seed, layer, _GAMMA).standard_normal(w.hidden), dtype=np.float32)
+
+
+def make_router(w: Workload, seed: int = 0, layer: int = 0) -> np.ndarray:
+    """Router weights of the MoE block, fp16 bit patterns [E][d] ~ fp16(N(0, 1/d)), so
+    that logits of a normalised input are ~N(0, 1) like the layer's own synthetic logits."""
+    a = _rng(seed, layer, _ROUTER).standard_normal((w.experts, w.hidden)) / np.sqrt(w.hidden)
+    return _half_bits(a)
+
+
+def make_gamma_pre(w: Workload, seed: int = 0, layer: int = 0) -> np.ndarray:
+    """Pre-norm weight of the MoE block, fp32 [d] ~ N(1, 0.1)."""
+    return np.ascontiguousarray(1.0 + 0.1 * _rng(seed, layer, _GAMMA_PRE).standard_normal(w.hidden), dtype=np.float32)
