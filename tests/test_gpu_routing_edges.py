@@ -30,7 +30,7 @@ def B():
     return binding
 
 
-def _route(B, lg, k):
+def _route(B, lg, k, repeats=1):
     T, E = lg.shape
     sh = B.make_shape(T, 128, 64, E, k, 64, 64)
     routing = B.RoutingBuffers(
@@ -41,14 +41,22 @@ def _route(B, lg, k):
     )
     ws = torch.empty((B.moe_w4a16_workspace_bytes(sh),), dtype=torch.uint8, device="cuda")
     B.moe_w4a16_workspace_init(ws)
-    B.moe_w4a16_route(sh, torch.from_numpy(np.ascontiguousarray(lg, np.float32)).cuda(), routing, ws)
-    torch.cuda.synchronize()
-    return tuple(t.cpu().numpy() for t in (routing.topk_idx, routing.topk_w, routing.expert_offsets,
-                                           routing.pair_list))
+    d_lg = torch.from_numpy(np.ascontiguousarray(lg, np.float32)).cuda()
+    runs = []
+    for _ in range(repeats):  # the same workspace: the one-launch routing's ticket must come back to 0
+        for t in (routing.topk_idx, routing.expert_offsets, routing.pair_list):
+            t.fill_(-1)
+        B.moe_w4a16_route(sh, d_lg, routing, ws)
+        torch.cuda.synchronize()
+        runs.append(tuple(t.cpu().numpy() for t in (routing.topk_idx, routing.topk_w, routing.expert_offsets,
+                                                    routing.pair_list)))
+    for r in runs[1:]:
+        assert all(np.array_equal(a, b) for a, b in zip(r, runs[0]))
+    return runs[0]
 
 
-def _check(B, lg, k):
-    idx_g, w_g, off_g, pl_g = _route(B, lg, k)
+def _check(B, lg, k, repeats=1):
+    idx_g, w_g, off_g, pl_g = _route(B, lg, k, repeats)
     idx_o, w_o = oracle.route(lg, k)
     off_o, pl_o = oracle.permute(idx_o, lg.shape[1])
     assert np.array_equal(idx_g, idx_o), np.argwhere(idx_g != idx_o)[:5]
@@ -110,3 +118,16 @@ def test_ragged_shapes_with_ties(B, T, E, k):
     rng = np.random.default_rng(T * 1000 + E)
     lg = rng.integers(-2, 3, (T, E)).astype(np.float32)
     _check(B, lg, k)
+
+
+@pytest.mark.parametrize("T,E,k", [(512, 128, 8), (513, 128, 8), (504, 256, 8), (1024, 128, 8), (4097, 256, 3),
+                                   (20000, 128, 8)])
+def test_one_launch_and_three_launch_routing(B, T, E, k):
+    """Up to 64 top-k CTAs (512 tokens) routing is one launch, whose last CTA groups
+    every pair; above that it takes three launches (top-k, per-expert prefix over
+    CTAs, placement).  Both sides of the boundary, and sizes far above it, against
+    the oracle, three calls each on one workspace."""
+    rng = np.random.default_rng(T + E + k)
+    lg = rng.standard_normal((T, E), dtype=np.float32)
+    lg[::7] = np.round(lg[::7])  # ties on some rows
+    _check(B, lg, k, repeats=3)

@@ -61,10 +61,15 @@ inline size_t ws_xs_offset(const Dims& s) { return (ws_h_offset() + ws_h_bytes(s
 inline size_t ws_xs_bytes(const Dims& s) { return size_t(s.pairs()) * s.d * 2; }
 inline size_t ws_y_offset(const Dims& s) { return (ws_xs_offset(s) + ws_xs_bytes(s) + 255) / 256 * 256; }
 inline size_t ws_y_bytes(const Dims& s) { return size_t(s.pairs()) * s.d * 4; }
-// routing scratch: per-CTA expert counts of the top-k launch (8 tokens per CTA), then the pairs' ranks
+// routing scratch: per-CTA expert counts of the top-k step (8 tokens per CTA), the pairs'
+// ranks, then the expert totals
 inline size_t ws_route_offset(const Dims& s) { return (ws_y_offset(s) + ws_y_bytes(s) + 255) / 256 * 256; }
-inline size_t ws_route_hist_bytes(const Dims& s) { return size_t((s.T + 7) / 8) * s.E * 4; }
-inline size_t ws_route_bytes(const Dims& s) { return ws_route_hist_bytes(s) + size_t(s.pairs()) * 4; }
+inline size_t ws_route_hist_bytes(const Dims& s) {  // rounded to 16 bytes: the ranks are read as vectors
+  return (size_t((s.T + 7) / 8) * s.E * 4 + 15) / 16 * 16;
+}
+inline size_t ws_route_bytes(const Dims& s) {
+  return ws_route_hist_bytes(s) + size_t(s.pairs()) * 4 + size_t(kMaxExperts) * 4;
+}
 // the MoE block's normalised input u (fp16 [T][d]) and router logits (fp32 [T][E])
 inline size_t ws_u_offset(const Dims& s) { return (ws_route_offset(s) + ws_route_bytes(s) + 255) / 256 * 256; }
 inline size_t ws_u_bytes(const Dims& s) { return size_t(s.T) * s.d * 2; }
