@@ -254,8 +254,15 @@ def test_sampler_invalid_configs_rejected(bad):
 def test_sampler_host_validation():
     cfg = B.make_sampler(**SAMPLER_VALID)
     need = B.moe_w4a16_sampler_workspace_bytes(cfg)
-    assert need == 8 * 1 * 32  # one 32-byte partial per position and vocabulary split of 32768
-    assert B.moe_w4a16_sampler_workspace_bytes(B.make_sampler(**dict(SAMPLER_VALID, vocab=262144))) == 8 * 8 * 32
+    def splits(P, V):  # about ceil(912 / P) splits, each a multiple of 2,048 elements
+        want = -(-912 // P)
+        chunk = -(-(-(-V // want)) // 2048) * 2048
+        return -(-V // chunk)
+    assert need == 8 * splits(8, 4096) * 32 == 8 * 2 * 32  # one 32-byte partial per position and split
+    for P, V, S in ((8, 262144, 64), (256, 262144, 4), (64, 262144, 15), (1024, 262144, 1), (1, 4, 1)):
+        assert splits(P, V) == S
+        assert B.moe_w4a16_sampler_workspace_bytes(B.make_sampler(**dict(SAMPLER_VALID, positions=P, vocab=V))) == \
+            P * S * 32
     L = B.lib()
     assert L.moe_w4a16_sample(None, 16, 16, 16, 16, 16, 16, 16, need, None) == B.ERR_NULL
     assert L.moe_w4a16_sample(ctypes.byref(cfg), None, 16, 16, 16, 16, 16, 16, need, None) == B.ERR_NULL

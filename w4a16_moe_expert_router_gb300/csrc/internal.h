@@ -152,11 +152,21 @@ cudaError_t launch_block_front(const Dims& s, const uint16_t* x, const float* ga
 // Per-step sampler (sampler.cu): one streaming pass over the logits (grid of
 // vocabulary splits x positions) writing 32-byte partials to the workspace, then
 // one CTA that merges them and applies the acceptance rule.
-constexpr int kSamplerChunk = 32768;        // vocabulary elements per CTA of the pass
 constexpr int kSamplerMaxPositions = 1024;  // one thread per position in the final CTA
-int sampler_splits(int64_t vocab);
+// Vocabulary elements per CTA of the pass: the vocabulary is cut into about
+// ceil(912 / positions) splits (912 CTAs: two waves of three 256-thread CTAs on
+// each of 152 SMs), each a multiple of 2,048 elements (one iteration of a CTA).
+// Fewer, longer CTAs amortise each CTA's start and final reduction.
+inline int64_t sampler_chunk(int positions, int64_t vocab) {
+  const int64_t want = (912 + positions - 1) / positions;
+  const int64_t per = (vocab + want - 1) / want;
+  return (per + 2047) / 2048 * 2048;
+}
+inline int sampler_splits(int positions, int64_t vocab) {
+  return static_cast<int>((vocab + sampler_chunk(positions, vocab) - 1) / sampler_chunk(positions, vocab));
+}
 inline size_t sampler_ws_bytes(int positions, int64_t vocab) {
-  return size_t(positions) * size_t(sampler_splits(vocab)) * 32;
+  return size_t(positions) * size_t(sampler_splits(positions, vocab)) * 32;
 }
 cudaError_t launch_sample(int P, int64_t V, float inv_temp, uint64_t seed, uint32_t step, int rule, float bound,
                           const float* logits, const uint8_t* revealed, int32_t* token, float* entropy, float* pmax,

@@ -29,10 +29,10 @@
 // exponentials included), and only the elements that pass it (a few per warp
 // over the pass) get their exact key.  The test reuses 2^(t2 - m2) of the
 // softmax sum, so an element costs one Philox quarter, one exp2 and about eight
-// other instructions.  The logits stream through an 8-stage cp.async ring in
-// shared memory (each thread copies and later reads its own float4 of every
-// stage, so the only wait is cp.async.wait_group on the thread's own copies and
-// no barrier is needed); seven 16-byte copies per thread are in flight.  Each CTA
+// other instructions.  A thread takes two float4s per iteration (eight elements,
+// one check of the screening factor) and loads them two iterations ahead with
+// streaming 16-byte loads into registers, so four loads per thread are in flight
+// and nothing waits on shared memory or a barrier.  Each CTA
 // writes its partial (m2, Z, S1, best key, index).
 //
 // Final kernel (one CTA, one thread per position): merges each position's
@@ -45,12 +45,12 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kPassThreads = 256;
-constexpr int kStages = 8;  // cp.async stages per thread: one float4 each, up to seven in flight
 constexpr int kFinalThreads = 1024;  // positions per call at most
 
 struct __align__(16) Partial {
@@ -166,7 +166,95 @@ __device__ __forceinline__ void merge_sums(float& m2, float& z, float& s1, float
   m2 = m;
 }
 
-__global__ void __launch_bounds__(kPassThreads, 4)
+// Running state of one pass thread.
+struct PassState {
+  float m2, z, s1;     // base-2 online softmax sums
+  float bk;            // best exact key so far, and its token
+  int32_t bv;
+  float c2, c_K, c_m2;  // screening factor and the (K, m2) it was made for
+};
+
+// Eight elements of one thread: float4s j and j + 256 of the CTA's range (ids
+// v0 + 4 j ...).  With kGuard, float4s at or past n4 take no part (the last
+// iteration of a range that is not a multiple of 512 float4s).
+template <bool kGuard>
+__device__ __forceinline__ void pass_iter(PassState& S, const float4 (&x)[2], int j, int n4, int64_t v0, uint32_t g0,
+                                          uint32_t p, uint32_t step, const PhiloxKeys& pk, float c2e, float inv_temp,
+                                          volatile uint32_t* vbest, uint32_t* cta_best) {
+  uint32_t w[2][4];
+  philox4x32_10(g0 + static_cast<uint32_t>(j), p, step, 0u, pk, w[0]);
+  philox4x32_10(g0 + static_cast<uint32_t>(j + kPassThreads), p, step, 0u, pk, w[1]);
+  const bool act[2] = {!kGuard || j < n4, !kGuard || j + kPassThreads < n4};
+  const float l[8] = {x[0].x, x[0].y, x[0].z, x[0].w, x[1].x, x[1].y, x[1].z, x[1].w};
+  float mx;
+  if (kGuard) {
+    mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (act[i / 4]) mx = fmaxf(mx, l[i]);
+  } else {
+    mx = fmaxf(fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3])), fmaxf(fmaxf(l[4], l[5]), fmaxf(l[6], l[7])));
+  }
+  mx *= c2e;
+  if (mx > S.m2) {
+    if (S.z != 0.f) {
+      const float dm = S.m2 - mx;
+      const float r = fast_exp2(dm);
+      S.s1 = r * fmaf(dm, S.z, S.s1);
+      S.z *= r;
+    }
+    S.m2 = mx;
+  }
+  // screen: element v needs w_v <= 2^(t2_v - K2 + slack) = 2^(t2_v - m2) c2 with
+  // c2 = 2^(m2 - K2 + slack); the slack (base-2 units) and the factor 1.01 cover
+  // the roundings of t2, K2 and the approximate exp2.  Before the CTA has a key,
+  // c2 is huge: every element whose 2^(t2 - m2) does not underflow is screened in
+  // (one that underflows cannot beat its thread's own maximum, which is screened in)
+  const float K = key_dec(*vbest);
+  if (K != S.c_K || S.m2 != S.c_m2) {
+    S.c_K = K;
+    S.c_m2 = S.m2;
+    S.c2 = 3e38f;
+    if (K != -INFINITY) {
+      const float K2 = K * 1.44269504088896341f;
+      const float slack = 0x1p-8f + (fabsf(S.m2) + fabsf(K2)) * 0x1p-14f;
+      S.c2 = fminf(fast_exp2(S.m2 - K2 + slack) * 1.01f, 3e38f);
+    }
+  }
+  bool cand[8];
+  bool any = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    cand[i] = false;
+    if (!act[i / 4]) continue;
+    const float d = fmaf(l[i], c2e, -S.m2);
+    const float e = fast_exp2(d);
+    S.z += e;
+    S.s1 = fmaf(e, d, S.s1);
+    // with f = 1 + (x & 0x7fffff) 2^-23, w = 1 - U = 2 - 2^-24 - f exactly, so
+    // w <= e c2  <=>  f >= 2 - 2^-24 - e c2, implied by f >= fl(2 - 2^-23 - e c2)
+    const float f = __uint_as_float(0x3f800000u | (w[i / 4][i % 4] & 0x007fffffu));
+    cand[i] = f >= fmaf(-e, S.c2, 0x1.fffffep+0f);
+    any |= cand[i];
+  }
+  if (__any_sync(0xffffffffu, any)) {
+    if (any) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (!cand[i]) continue;
+        const float k = gumbel_key(l[i], inv_temp, w[i / 4][i % 4]);
+        const int32_t v = static_cast<int32_t>(v0 + 4 * static_cast<int64_t>(j + (i / 4) * kPassThreads) + i % 4);
+        if (better(k, v, S.bk, S.bv)) {
+          S.bk = k;
+          S.bv = v;
+        }
+      }
+      atomicMax(cta_best, key_enc(S.bk));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kPassThreads, 3)
     sample_pass_kernel(const float* __restrict__ logits, int64_t V, int chunk, float inv_temp, uint32_t k0,
                        uint32_t k1, uint32_t step, Partial* __restrict__ part) {
   __shared__ uint32_t cta_best;  // encoded best exact key of the CTA so far
@@ -175,99 +263,63 @@ __global__ void __launch_bounds__(kPassThreads, 4)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x, p = blockIdx.y;
   if (tid == 0) cta_best = key_enc(-INFINITY);
+  grid_dependents_launch();  // the final launch may set up meanwhile; it waits for this one
+  grid_dependency_wait();    // the logits of the launch before
   __syncthreads();
   const int64_t v0 = static_cast<int64_t>(s) * chunk;
-  const int64_t n4 = (min(V, v0 + chunk) - v0) / 4;
+  const int n4 = static_cast<int>((min(V, v0 + chunk) - v0) / 4);
   const float4* src = reinterpret_cast<const float4*>(logits + static_cast<int64_t>(p) * V + v0);
   const uint32_t g0 = static_cast<uint32_t>(v0 / 4);
   const float c2e = inv_temp * 1.44269504088896341f;  // screening only
-  volatile uint32_t* vbest = &cta_best;
-  float m2 = -INFINITY, z = 0.f, s1 = 0.f;
-  float bk = -INFINITY;
-  int32_t bv = 0x7fffffff;
-  __shared__ float4 ring[kStages][kPassThreads];
   const PhiloxKeys pk = philox_keys(k0, k1);
-  const int n_iter = static_cast<int>((n4 + kPassThreads - 1) / kPassThreads);
-  // copy of float4 (it * 256 + tid) into slot it % kStages; one commit group per iteration
-  auto issue = [&](int it) {
-    const int64_t j = static_cast<int64_t>(it) * kPassThreads + tid;
-    if (it < n_iter && j < n4) {
-      const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&ring[it % kStages][tid]));
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + j) : "memory");
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  };
+  PassState S{-INFINITY, 0.f, 0.f, -INFINITY, 0x7fffffff, 3e38f, NAN, NAN};
+  // iteration it covers float4s j = it * 512 + tid and j + 256; the loads run two
+  // iterations ahead, streaming (evict-first), from addresses clamped into the range
+  // (a load past its end is never used)
+  constexpr int kStep = 2 * kPassThreads;
+  const int n_full = n4 / kStep, n_iter = (n4 + kStep - 1) / kStep;
+  const int last4 = max(n4 - 1, 0);
+  auto load = [&](int j) { return __ldcs(src + min(j, last4)); };
+  float4 cur[2] = {load(tid), load(tid + kPassThreads)};
+  float4 nxt[2] = {load(kStep + tid), load(kStep + tid + kPassThreads)};
+  {
+    // a first threshold for the screen: the exact key of each thread's largest logit
+    // among its first eight (any element's exact key is a valid threshold; without
+    // one, every element of the first iteration would need its exact key)
+    const float l[8] = {cur[0].x, cur[0].y, cur[0].z, cur[0].w, cur[1].x, cur[1].y, cur[1].z, cur[1].w};
+    int ib = -1;
 #pragma unroll
-  for (int it = 0; it < kStages - 1; ++it) issue(it);
-  float c2 = 3e38f, c_K = NAN, c_m2 = NAN;  // screening factor and the (K, m2) it was made for
-  for (int it = 0; it < n_iter; ++it) {  // uniform trip count
-    issue(it + kStages - 1);
-    asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");  // this thread's copy of `it` landed
-    const int64_t j = static_cast<int64_t>(it) * kPassThreads + tid;
-    const bool active = j < n4;
-    float4 l4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (active) l4 = ring[it % kStages][tid];
-    uint32_t w[4];
-    philox4x32_10(g0 + static_cast<uint32_t>(j), static_cast<uint32_t>(p), step, 0u, pk, w);
-    const float l[4] = {l4.x, l4.y, l4.z, l4.w};
-    bool cand[4] = {false, false, false, false};
-    if (active) {
-      const float mx = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3])) * c2e;
-      if (mx > m2) {
-        if (z != 0.f) {
-          const float dm = m2 - mx;
-          const float r = fast_exp2(dm);
-          s1 = r * fmaf(dm, z, s1);
-          z *= r;
-        }
-        m2 = mx;
-      }
-      // screen: element v needs w_v <= 2^(t2_v - K2 + slack) = 2^(t2_v - m2) c2 with
-      // c2 = 2^(m2 - K2 + slack); the slack (base-2 units) and the factor 1.01 cover
-      // the roundings of t2, K2 and the approximate exp2.  Before the CTA has a key,
-      // c2 is huge: every element whose 2^(t2 - m2) does not underflow is screened in
-      // (one that underflows cannot beat its thread's own maximum, which is screened in)
-      const float K = key_dec(*vbest);
-      if (K != c_K || m2 != c_m2) {
-        c_K = K;
-        c_m2 = m2;
-        c2 = 3e38f;
-        if (K != -INFINITY) {
-          const float K2 = K * 1.44269504088896341f;
-          const float slack = 0x1p-8f + (fabsf(m2) + fabsf(K2)) * 0x1p-14f;
-          c2 = fminf(fast_exp2(m2 - K2 + slack) * 1.01f, 3e38f);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float d = fmaf(l[i], c2e, -m2);
-        const float e = fast_exp2(d);
-        z += e;
-        s1 = fmaf(e, d, s1);
-        // with f = 1 + (x & 0x7fffff) 2^-23, w = 1 - U = 2 - 2^-24 - f exactly, so
-        // w <= e c2  <=>  f >= 2 - 2^-24 - e c2, implied by f >= fl(2 - 2^-23 - e c2)
-        const float f = __uint_as_float(0x3f800000u | (w[i] & 0x007fffffu));
-        cand[i] = f >= fmaf(-e, c2, 0x1.fffffep+0f);
-      }
+    for (int i = 0; i < 8; ++i)
+      if (tid + (i / 4) * kPassThreads < n4 && (ib < 0 || l[i] > l[ib])) ib = i;
+    if (ib >= 0) {
+      const int j = tid + (ib / 4) * kPassThreads;
+      uint32_t w[4];
+      philox4x32_10(g0 + static_cast<uint32_t>(j), static_cast<uint32_t>(p), step, 0u, pk, w);
+      const float lb = ib == 0 ? l[0] : ib == 1 ? l[1] : ib == 2 ? l[2] : ib == 3 ? l[3]
+                     : ib == 4 ? l[4] : ib == 5 ? l[5] : ib == 6 ? l[6] : l[7];
+      const uint32_t wb = (ib & 3) == 0 ? w[0] : (ib & 3) == 1 ? w[1] : (ib & 3) == 2 ? w[2] : w[3];
+      S.bk = gumbel_key(lb, inv_temp, wb);
+      S.bv = static_cast<int32_t>(v0 + 4 * static_cast<int64_t>(j) + (ib & 3));
+      atomicMax(&cta_best, key_enc(S.bk));
     }
-    const bool any = cand[0] || cand[1] || cand[2] || cand[3];
-    if (__any_sync(0xffffffffu, any)) {
-      if (any) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (!cand[i]) continue;
-          const float k = gumbel_key(l[i], inv_temp, w[i]);
-          const int32_t v = static_cast<int32_t>(v0 + 4 * j + i);
-          if (better(k, v, bk, bv)) {
-            bk = k;
-            bv = v;
-          }
-        }
-        atomicMax(&cta_best, key_enc(bk));
-      }
-    }
+    __syncthreads();
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
+  int it = 0;
+  for (; it < n_full; ++it) {  // uniform trip count
+    const int j = it * kStep + tid;
+    const float4 pf0 = load(j + 2 * kStep), pf1 = load(j + 2 * kStep + kPassThreads);
+    pass_iter<false>(S, cur, j, n4, v0, g0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp, &cta_best,
+                     &cta_best);
+    cur[0] = nxt[0];
+    cur[1] = nxt[1];
+    nxt[0] = pf0;
+    nxt[1] = pf1;
+  }
+  if (it < n_iter)  // the range's last, partial iteration
+    pass_iter<true>(S, cur, it * kStep + tid, n4, v0, g0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp,
+                    &cta_best, &cta_best);
+  float m2 = S.m2, z = S.z, s1 = S.s1, bk = S.bk;
+  int32_t bv = S.bv;
   // reduce: sums and the best (key, index), lanes then warps in a fixed order
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -309,33 +361,51 @@ __global__ void __launch_bounds__(kPassThreads, 4)
   }
 }
 
+// Order-preserving encoding of an entropy for the ascending sort (-0 as +0, so
+// that equal values tie and fall back to the position, as fp32 comparison does).
+__device__ __forceinline__ uint32_t asc_enc(float h) {
+  const uint32_t b = __float_as_uint(h == 0.f ? 0.f : h);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float asc_dec(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
 __global__ void __launch_bounds__(kFinalThreads)
     sample_final_kernel(const Partial* __restrict__ part, int P, int S, int rule, float bound,
                         const uint8_t* __restrict__ revealed, int32_t* __restrict__ token, float* __restrict__ entropy,
                         float* __restrict__ pmax, uint8_t* __restrict__ accept) {
-  __shared__ __align__(16) float sh_h[kFinalThreads];
-  __shared__ __align__(16) float sh_pm[kFinalThreads];
-  __shared__ __align__(16) float sorted_h[kFinalThreads];
-  __shared__ __align__(16) int sorted_p[kFinalThreads];
-  __shared__ __align__(16) uint8_t sh_rev[kFinalThreads];
+  __shared__ unsigned long long keys[kFinalThreads];  // rule 0: (entropy, position), sorted ascending
+  __shared__ float red_pm[kFinalThreads / 32];
+  __shared__ int red_q[kFinalThreads / 32];
   __shared__ uint8_t sh_acc[kFinalThreads];
-  const int p = threadIdx.x;
-  // positions past P take part as revealed, with an entropy that ranks last
+  grid_dependency_wait();  // the pass launch's partials
+  const int p = threadIdx.x, lane = p & 31, warp = p >> 5;
   float h = INFINITY, pm = 0.f;
-  uint8_t rev = 1;
+  bool rev = true;  // positions past P take part as revealed
   if (p < P) {
+    // merge the position's partials in split order (loads four at a time ahead of the merges)
     const float4* q = reinterpret_cast<const float4*>(part + static_cast<int64_t>(p) * S);
-    float4 a = __ldg(q);
-    float m2 = a.x, z = a.y, s1 = a.z, bk = a.w;
-    int32_t bv = __float_as_int(__ldg(q + 1).x);
-    for (int i = 1; i < S; ++i) {
-      const float4 b = __ldg(q + 2 * i);
-      const int32_t v = __float_as_int(__ldg(q + 2 * i + 1).x);
-      merge_sums(m2, z, s1, b.x, b.y, b.z);
-      if (better(b.w, v, bk, bv)) {
-        bk = b.w;
-        bv = v;
-      }
+    float m2 = -INFINITY, z = 0.f, s1 = 0.f, bk = -INFINITY;
+    int32_t bv = 0x7fffffff;
+    for (int i0 = 0; i0 < S; i0 += 4) {
+      float4 a[4];
+      int32_t v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u < S) {
+          a[u] = __ldg(q + 2 * (i0 + u));
+          v[u] = __float_as_int(__ldg(q + 2 * (i0 + u) + 1).x);
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u < S) {
+          merge_sums(m2, z, s1, a[u].x, a[u].y, a[u].z);
+          if (better(a[u].w, v[u], bk, bv)) {
+            bk = a[u].w;
+            bv = v[u];
+          }
+        }
     }
     h = logf(z) - (s1 / z) * 0.693147180559945309f;
     pm = 1.f / z;
@@ -344,62 +414,85 @@ __global__ void __launch_bounds__(kFinalThreads)
     entropy[p] = h;
     pmax[p] = pm;
   }
-  sh_h[p] = h;
-  sh_pm[p] = pm;
-  sh_rev[p] = rev;
   sh_acc[p] = 0;
-  const int n = __syncthreads_count(!rev);  // unrevealed positions
-  const int P4 = (P + 3) & ~3;              // rank over whole float4s: padded slots are revealed
-  if (rule == 0) {
-    // rank of each unrevealed position by (entropy, position)
-    if (!rev) {
-      int r = 0;
-      for (int q = 0; q < P4; q += 4) {
-        const float4 hq = *reinterpret_cast<const float4*>(&sh_h[q]);
-        const uchar4 rq = *reinterpret_cast<const uchar4*>(&sh_rev[q]);
-        r += !rq.x && (hq.x < h || (hq.x == h && q < p));
-        r += !rq.y && (hq.y < h || (hq.y == h && q + 1 < p));
-        r += !rq.z && (hq.z < h || (hq.z == h && q + 2 < p));
-        r += !rq.w && (hq.w < h || (hq.w == h && q + 3 < p));
+  if (rule == 1) {
+    // confidence: every unrevealed position above the threshold; if none, the
+    // unrevealed one with the largest pmax (ties to the lower position)
+    const bool acc = !rev && pm > bound;
+    const int any = __syncthreads_or(acc);
+    if (any) {
+      if (p < P) accept[p] = acc;
+      return;
+    }
+    float bpm = rev ? -1.f : pm;
+    int bq = rev ? 0x7fffffff : p;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float opm = __shfl_xor_sync(0xffffffffu, bpm, off);
+      const int oq = __shfl_xor_sync(0xffffffffu, bq, off);
+      if (opm > bpm || (opm == bpm && oq < bq)) {
+        bpm = opm;
+        bq = oq;
       }
-      sorted_h[r] = h;
-      sorted_p[r] = p;
+    }
+    if (lane == 0) {
+      red_pm[warp] = bpm;
+      red_q[warp] = bq;
     }
     __syncthreads();
     if (p == 0) {
-      // the mlx-vlm rule in sorted order, one fp32 rounding per step, in sequence
-      float c = 0.f, x = -INFINITY;
-      int i = 0;
-      for (; i + 4 <= n; i += 4) {
-        const float4 hv = *reinterpret_cast<const float4*>(&sorted_h[i]);
-        const int4 pv = *reinterpret_cast<const int4*>(&sorted_p[i]);
-        const float hh[4] = {hv.x, hv.y, hv.z, hv.w};
-        const int pp[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          c = __fadd_rn(c, hh[u]);
-          x = fmaxf(x, hh[u]);
-          if (i + u == 0 || __fsub_rn(c, x) <= bound) sh_acc[pp[u]] = 1;
+      for (int w = 1; w < kFinalThreads / 32; ++w)
+        if (red_pm[w] > red_pm[0] || (red_pm[w] == red_pm[0] && red_q[w] < red_q[0])) {
+          red_pm[0] = red_pm[w];
+          red_q[0] = red_q[w];
         }
+      if (red_q[0] < P) sh_acc[red_q[0]] = 1;
+    }
+  } else {
+    // entropy bound: sort the unrevealed positions by (entropy, position) (bitonic, over
+    // the next power of two >= P), then one thread applies the rule in sorted order with
+    // one fp32 rounding per step
+    int n2 = 32;
+    while (n2 < P) n2 <<= 1;
+    keys[p] = rev ? ~0ull : (static_cast<unsigned long long>(asc_enc(h)) << 32) | static_cast<uint32_t>(p);
+    const int n = __syncthreads_count(!rev);
+    for (int k = 2; k <= n2; k <<= 1)
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        // a stage with j < 32 pairs lanes of one warp: the warp's own barrier orders it
+        if (j >= 32) __syncthreads();
+        const int q2 = p ^ j;
+        if (p < n2 && q2 > p) {
+          const unsigned long long a = keys[p], b = keys[q2];
+          if (((p & k) == 0) == (a > b)) {
+            keys[p] = b;
+            keys[q2] = a;
+          }
+        }
+        if (j >= 32) __syncthreads();
+        else __syncwarp();
       }
-      for (; i < n; ++i) {
-        c = __fadd_rn(c, sorted_h[i]);
-        x = fmaxf(x, sorted_h[i]);
-        if (i == 0 || __fsub_rn(c, x) <= bound) sh_acc[sorted_p[i]] = 1;
+    __syncthreads();
+    if (warp == 0) {
+      // warp 0 walks the sorted entries 32 at a time: lane u loads entry i0 + u, every
+      // lane runs the same sequence of fp32 sums and maxima over the broadcast values,
+      // and lane u keeps the decision for its own entry
+      float c = 0.f, x = -INFINITY;
+      for (int i0 = 0; i0 < n; i0 += 32) {
+        const unsigned long long kk = keys[min(i0 + lane, kFinalThreads - 1)];
+        const float hl = asc_dec(static_cast<uint32_t>(kk >> 32));
+        bool mine = false;
+#pragma unroll 8
+        for (int u = 0; u < 32; ++u) {
+          if (i0 + u >= n) break;
+          const float hu = __shfl_sync(0xffffffffu, hl, u);
+          c = __fadd_rn(c, hu);
+          x = fmaxf(x, hu);
+          const bool ok = i0 + u == 0 || __fsub_rn(c, x) <= bound;
+          if (u == lane) mine = ok;
+        }
+        if (mine && i0 + lane < n) sh_acc[static_cast<uint32_t>(kk)] = 1;
       }
     }
-  } else if (p == 0) {
-    int best = -1;
-    bool any = false;
-    for (int q = 0; q < P; ++q) {
-      if (sh_rev[q]) continue;
-      if (sh_pm[q] > bound) {
-        sh_acc[q] = 1;
-        any = true;
-      }
-      if (best < 0 || sh_pm[q] > sh_pm[best]) best = q;
-    }
-    if (!any && best >= 0) sh_acc[best] = 1;
   }
   __syncthreads();
   if (p < P) accept[p] = sh_acc[p];
@@ -407,20 +500,18 @@ __global__ void __launch_bounds__(kFinalThreads)
 
 }  // namespace
 
-int sampler_splits(int64_t vocab) { return static_cast<int>((vocab + kSamplerChunk - 1) / kSamplerChunk); }
 
 cudaError_t launch_sample(int P, int64_t V, float inv_temp, uint64_t seed, uint32_t step, int rule, float bound,
                           const float* logits, const uint8_t* revealed, int32_t* token, float* entropy, float* pmax,
                           uint8_t* accept, void* workspace, cudaStream_t st) {
-  const int S = sampler_splits(V);
+  const int S = sampler_splits(P, V);
+  const int chunk = static_cast<int>(sampler_chunk(P, V));
   auto* part = static_cast<Partial*>(workspace);
-  sample_pass_kernel<<<dim3(S, P), kPassThreads, 0, st>>>(logits, V, kSamplerChunk, inv_temp,
-                                                          static_cast<uint32_t>(seed),
-                                                          static_cast<uint32_t>(seed >> 32), step, part);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(sample_pass_kernel, dim3(S, P), dim3(kPassThreads), 0, st, logits, V, chunk,
+                             inv_temp, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), step, part);
   if (e != cudaSuccess) return e;
-  sample_final_kernel<<<1, kFinalThreads, 0, st>>>(part, P, S, rule, bound, revealed, token, entropy, pmax, accept);
-  return cudaGetLastError();
+  return launch_pdl(sample_final_kernel, dim3(1), dim3(kFinalThreads), 0, st, static_cast<const Partial*>(part), P, S,
+                    rule, bound, revealed, token, entropy, pmax, accept);
 }
 
 }  // namespace moe
