@@ -11,7 +11,10 @@ library's C ABI on device-resident inputs.  Prints one JSON line (rank 0).
 
 `--sampler` times the per-step sampler instead (entropy, Gumbel-max token and
 acceptance over the fp32 logits of a 256-position canvas with a 262,144-token
-vocabulary: 268 MB per step) and prints its own JSON line.
+vocabulary: 268 MB per step) and prints its own JSON line.  `--block` times the
+whole MoE block per layer instead (pre-norm and router projection of x, then
+the layer, the residual added in the combine) as one moe_w4a16_block call; the
+router logits are then formed on the device, not an input.
 
 Under torchrun every rank runs its own canvas on its own GPU (independent
 problems, no collective on the data path): weak scaling; value = tokens of all
@@ -58,6 +61,9 @@ def parse_args(argv=None):
                    help="replay each step from a CUDA graph captured once (per weight copy) instead of launching it")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--sampler", action="store_true", help="time the per-step sampler instead of the layer")
+    p.add_argument("--block", action="store_true",
+                   help="time the whole MoE block per layer (pre-norm, router projection, routing, experts, "
+                        "combine with the residual) as one moe_w4a16_block call; logits are not an input")
     return p.parse_args(argv)
 
 
@@ -223,6 +229,11 @@ def run_ours(args, rank, world, local):
             weights.append(runtime.PreparedWeights(torch.from_numpy(gu).to(dev), torch.from_numpy(dn).to(dev)))
         gammas.append(runtime.to_device_f32(synth.make_gamma(wl, 0, layer=l), dev) if wl.rmsnorm else None)
         del w, gu, dn
+    if args.block:  # the block's own router weights and pre-norm weight, per layer
+        if wl.rmsnorm:
+            raise SystemExit("--block takes a workload without the layer-stack RMSNorm (the block is pre-norm)")
+        routers = [runtime.to_device_u16(synth.make_router(wl, 0, layer=l), dev) for l in range(layers)]
+        gammas_pre = [runtime.to_device_f32(synth.make_gamma_pre(wl, 0, layer=l), dev) for l in range(layers)]
     # a dedicated stream (a CUDA graph cannot capture the legacy default stream)
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
@@ -241,9 +252,19 @@ def run_ours(args, rank, world, local):
     shp, rp = ctypes.byref(sh), ctypes.byref(r)
 
     def layer_calls(l, src, dst, w_i, evs=None):
-        """route, experts (gate_up + down in one launch), combine of layer l; events between the calls if given."""
+        """route, experts (gate_up + down in one launch), combine of layer l; events between the calls if given.
+        With --block: the one moe_w4a16_block call of layer l (its events all after the call)."""
         if evs is not None:
             evs[0].record(stream)
+        if args.block:
+            st = L.moe_w4a16_block(shp, src.data_ptr(), gammas_pre[l].data_ptr(), 1e-6, routers[l].data_ptr(), rp,
+                                   ctypes.byref(wstructs[w_i]), dst.data_ptr(), ws_ptr, ws_n, sptr)
+            if evs is not None:
+                for e in evs[1:]:
+                    e.record(stream)
+            if st:
+                raise RuntimeError(f"library call failed with status {st}")
+            return
         st = L.moe_w4a16_route(shp, lg[l].data_ptr(), rp, ws_ptr, ws_n, sptr)
         if evs is not None:
             evs[1].record(stream)
@@ -269,7 +290,10 @@ def run_ours(args, rank, world, local):
 
     # routing statistics for the algorithmic byte count (per layer: experts touched)
     for l in range(layers):
-        B.moe_w4a16_route(sh, lg[l], buf.routing, buf.workspace, stream)
+        if args.block:
+            layer_calls(l, x, outs[0], l * copies)
+        else:
+            B.moe_w4a16_route(sh, lg[l], buf.routing, buf.workspace, stream)
         off = buf.routing.expert_offsets.cpu().numpy()
         touched.append(int(np.count_nonzero(np.diff(off))))
     d, f, g1, g2 = wl.hidden, wl.inter, wl.group_gate_up, wl.group_down
@@ -341,7 +365,7 @@ def run_ours(args, rank, world, local):
     ms_per_step = max_ms / K
     peak, peak_src = measured_peak()
     # the expert launch streams every touched expert's weights of both projections once
-    achieved = (layer_bytes / layers) / (experts_us * 1e-6) / 1e9
+    achieved = (layer_bytes / layers) / ((route_us if args.block else experts_us) * 1e-6) / 1e9
     layer_gbs = layer_bytes / (ms_per_step * 1e-3) / 1e9
 
     # end to end through the public API: pinned host buffers, copies inside the timed region
@@ -355,6 +379,15 @@ def run_ours(args, rank, world, local):
     def e2e_step(i):
         x_in.copy_(x_host, non_blocking=True)
         src = x_in
+        if args.block:
+            for l in range(layers):
+                dst = outs[l % 2]
+                wts = weights[l * copies + (i % copies)]
+                B.moe_w4a16_block(sh, src, gammas_pre[l], 1e-6, routers[l], buf.routing, wts.gate_up, wts.down, dst,
+                                  buf.workspace, stream)
+                src = dst
+            out_host.copy_(src, non_blocking=True)
+            return
         for l in range(layers):
             lg_in[l].copy_(lg_host[l], non_blocking=True)
             dst = outs[l % 2]
@@ -376,7 +409,7 @@ def run_ours(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    h2d = x_bits.nbytes + sum(a.nbytes for a in logits)
+    h2d = x_bits.nbytes + (0 if args.block else sum(a.nbytes for a in logits))
     d2h = wl.tokens * wl.hidden * 2
 
     result = {
@@ -395,7 +428,7 @@ def run_ours(args, rank, world, local):
         "dtype": "f16",
         "data": "synthetic",
         "config": {
-            "workload": wl.name, "tokens": wl.tokens, "hidden": wl.hidden, "inter": wl.inter,
+            "workload": wl.name + ("_block" if args.block else ""), "tokens": wl.tokens, "hidden": wl.hidden, "inter": wl.inter,
             "experts": wl.experts, "top_k": wl.top_k, "group_gate_up": wl.group_gate_up,
             "group_down": wl.group_down, "layers": layers, "rmsnorm": wl.rmsnorm,
             "reduction": wl.reduction, "weight_format": wl.format,
@@ -407,23 +440,29 @@ def run_ours(args, rank, world, local):
         },
         "hbm_gbs": layer_gbs,
         "hbm_frac_of_peak": layer_gbs / peak,
-        "kernel_us": {"route": route_us, "experts": experts_us, "combine": comb_us},
+        "kernel_us": {"block": route_us} if args.block else {"route": route_us, "experts": experts_us,
+                                                              "combine": comb_us},
         "roofline": {
-            "kernel": "expert_gemm_mma_kernel (gate_up + down grouped dequant GEMMs in one persistent launch: "
+            "kernel": ("the whole moe_w4a16_block call (pre-norm and router projection, routing, row copy, "
+                       "expert GEMMs, combine with the residual): the expert weights' bytes over the call's time")
+            if args.block else
+                      "expert_gemm_mma_kernel (gate_up + down grouped dequant GEMMs in one persistent launch: "
                       "TMA/bulk-copy ring, in-register dequant, m16n8k16 tensor-core MMAs; its timed segment also "
                       "holds the expert-order row copy launched before it)",
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "peak_source": peak_src,
             # the committed counters are of the default instantiation on canvas256
-            "traffic": profiled_traffic() if (wl.name, wl.reduction, wl.format) == ("canvas256", 0, 0) else None,
+            "traffic": profiled_traffic() if (wl.name, wl.reduction, wl.format, args.block) == ("canvas256", 0, 0, False)
+            else None,
             "algorithmic_bytes_per_launch": layer_bytes / layers,
         },
         "e2e": {"value": wl.tokens * KE * world / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE},
-        "gpu_launches": K * layers * 5,  # top-k, grouping, row copy, expert GEMMs, combine
+        # (pre-norm + router projection,) top-k, grouping, row copy, expert GEMMs, combine
+        "gpu_launches": K * layers * (6 if args.block else 5),
         "clocks": clocks.summary(),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.block:
         result["cpu_baseline"] = cpu_baseline(wl)
         result["cpu_baseline_1core"] = cpu_baseline(wl, nthreads=1)
     return result
