@@ -75,13 +75,15 @@ def _check(lg, revealed, inv_temp, rule, bound, seed, step, got):
 
 @pytest.mark.parametrize("P,V,sigma,inv_temp,rule,bound", [
     (8, 4096, 1.0, 1.0, 0, 5.0),
-    (3, 4100, 3.0, 0.7, 1, 0.5),          # one split, vocabulary not a multiple of the thread stride
-    (5, 70000, 1.0, 1.0, 0, 30.0),        # three splits (32,768 each), ragged last split
-    (1, 4, 2.0, 1.3, 0, 0.0),             # smallest vocabulary
-    (17, 65544, 3.0, 1.0, 1, 0.9),        # two full splits and 8 elements
+    (3, 4100, 3.0, 0.7, 1, 0.5),          # splits of 2,048: two full ones and a split of one float4
+    (5, 70000, 1.0, 1.0, 0, 30.0),        # ragged last split
+    (1, 4, 2.0, 1.3, 0, 0.0),             # smallest vocabulary: one split of one float4
+    (17, 65544, 3.0, 1.0, 1, 0.9),        # 32 full splits of 2,048 and one of 8 elements
     (64, 32768, 1.0, 2.0, 0, 1.0),
-    (6, 32772, 1.0, 1.0, 0, 2.0),         # one full split and a split of one float4
-    (9, 2060, 3.0, 1.0, 0, 3.0),          # one full iteration (512 float4s) and a partial one of 3
+    (6, 32772, 1.0, 1.0, 0, 2.0),
+    (9, 2060, 3.0, 1.0, 0, 3.0),          # a split of one full iteration (512 float4s) and one of 12 elements
+    (1, 1000000, 1.0, 1.0, 0, 2.0),       # one position cut into 489 splits: many partials to merge
+    (3, 999996, 3.0, 1.0, 1, 0.5),        # 245 splits of 4,096 per position, the last one ragged
 ], ids=lambda v: str(v))
 def test_sampler_matches_oracle(B, P, V, sigma, inv_temp, rule, bound):
     lg = _logits(P, V, sigma, seed=P * 1000 + V)
