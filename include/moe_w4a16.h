@@ -356,14 +356,23 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_unprepare(const moe_w4a16_shape* shape,
  *     other and give undefined results.  Each call clears the array's work
  *     counters when it starts; the rest keeps the last call's contents until
  *     overwritten.
- *   - A device-side wait that runs out is not reported (the error word sits in
- *     the static array); such a call's output is invalid.
+ *   - A device-side wait that runs out records MOE_W4A16_ERR_TIMEOUT in the
+ *     static array's error word (the call's output is then invalid);
+ *     moe_w4a16_noalloc_read_error reads that word back.
  * Arguments are those of moe_w4a16_forward, without the workspace. */
 #define MOE_W4A16_NOALLOC_SCRATCH_BYTES ((size_t)40 << 20)
 MOE_W4A16_API moe_w4a16_status moe_w4a16_forward_noalloc(const moe_w4a16_shape* shape, const uint16_t* x,
                                                          const moe_w4a16_routing* routing,
                                                          const moe_w4a16_weights* weights, const float* norm_gamma,
                                                          float norm_eps, uint16_t* out, void* stream);
+
+/* Copies the error word of the current device's static array to
+ * *device_status after synchronising `stream`: MOE_W4A16_OK, or the status of a
+ * device-side failure of the last moe_w4a16_forward_noalloc call on this device
+ * (each such call clears the word when it starts).  Errors: ERR_NULL for a NULL
+ * device_status, ERR_DEVICE on a device other than compute capability 10.3,
+ * ERR_CUDA if the copy fails. */
+MOE_W4A16_API moe_w4a16_status moe_w4a16_noalloc_read_error(void* stream, moe_w4a16_status* device_status);
 
 /* Self-test of the device-side failure path.  Every wait in the expert launch
  * (on its mbarrier rings and on the counters other CTAs raise) is bounded: on

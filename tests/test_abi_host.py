@@ -126,6 +126,10 @@ def test_block_validation_before_any_launch():
     assert B.moe_w4a16_workspace_bytes(sh) >= 16 * 256 * 2 + 16 * 8 * 4  # room for u and the logits
 
 
+def test_noalloc_read_error_checks_its_pointer():
+    assert B.lib().moe_w4a16_noalloc_read_error(None, None) == B.ERR_NULL
+
+
 def test_zero_tokens_is_a_no_op():
     L = B.lib()
     sh = _shape(tokens=0)

@@ -73,6 +73,8 @@ def test_noalloc_bit_identical_full_size(rt, name):
     _, _, _, _, dw, buf, xd, gd, ref = _case(rt, wl, 5, False)
     for out in _noalloc_twice(buf, xd, dw, gd, ref):
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    from w4a16_moe_expert_router_gb300 import binding as B
+    assert B.moe_w4a16_noalloc_read_error() == B.OK  # the device-side status of the last call
 
 
 def test_noalloc_against_the_oracle(rt):

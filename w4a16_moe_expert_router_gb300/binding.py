@@ -27,7 +27,7 @@ EXPORTED = ("moe_w4a16_workspace_bytes", "moe_w4a16_workspace_init", "moe_w4a16_
             "moe_w4a16_gate_up", "moe_w4a16_down", "moe_w4a16_combine", "moe_w4a16_read_error", "moe_w4a16_pack", "moe_w4a16_unpack", "moe_w4a16_prepared_bytes",
             "moe_w4a16_prepare", "moe_w4a16_unprepare", "moe_w4a16_status_string", "moe_w4a16_forward_noalloc",
             "moe_w4a16_selftest_wait_timeout", "moe_w4a16_sampler_workspace_bytes", "moe_w4a16_sample",
-            "moe_w4a16_block_front", "moe_w4a16_block")
+            "moe_w4a16_block_front", "moe_w4a16_block", "moe_w4a16_noalloc_read_error")
 
 NOALLOC_SCRATCH_BYTES = 40 << 20  # MOE_W4A16_NOALLOC_SCRATCH_BYTES
 
@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
             L.moe_w4a16_block.argtypes = [P(Shape), vp, vp, ctypes.c_float, vp, P(Routing), P(Weights), vp, vp, sz,
                                           vp]
             L.moe_w4a16_block.restype = st
+            L.moe_w4a16_noalloc_read_error.argtypes = [vp, P(ctypes.c_int32)]
+            L.moe_w4a16_noalloc_read_error.restype = st
             L.moe_w4a16_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint64, vp]
             L.moe_w4a16_selftest_wait_timeout.restype = st
             L.moe_w4a16_sampler_workspace_bytes.argtypes = [P(Sampler)]
@@ -224,6 +226,14 @@ def moe_w4a16_forward_noalloc(shape: Shape, x, routing: RoutingBuffers, gate_up,
     _check(lib().moe_w4a16_forward_noalloc(ctypes.byref(shape), _dptr(x), ctypes.byref(r), ctypes.byref(w),
                                            _dptr(norm_gamma), float(norm_eps), _dptr(out), _stream(stream)),
            "moe_w4a16_forward_noalloc")
+
+
+def moe_w4a16_noalloc_read_error(stream=None) -> int:
+    """The error word of the current device's static scratch (the last
+    allocation-free call's device-side status)."""
+    code = ctypes.c_int32(0)
+    _check(lib().moe_w4a16_noalloc_read_error(_stream(stream), ctypes.byref(code)), "moe_w4a16_noalloc_read_error")
+    return code.value
 
 
 def moe_w4a16_experts(shape: Shape, x, routing: RoutingBuffers, gate_up, down, workspace, stream=None) -> None:

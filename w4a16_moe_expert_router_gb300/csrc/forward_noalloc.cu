@@ -77,3 +77,20 @@ extern "C" moe_w4a16_status moe_w4a16_forward_noalloc(const moe_w4a16_shape* sha
   return moe::forward_all_steps(shape, x, routing, weights, norm_gamma, norm_eps, out, scratch, kScratchBytes, stream,
                                 true);
 }
+
+// The sticky error word at the start of this device's static array: the status of
+// device-side failures of the last moe_w4a16_forward_noalloc call on the device
+// (each call clears it when it starts).  Synchronises the stream.
+extern "C" moe_w4a16_status moe_w4a16_noalloc_read_error(void* stream, moe_w4a16_status* device_status) {
+  if (!device_status) return MOE_W4A16_ERR_NULL;
+  void* scratch = nullptr;
+  moe_w4a16_status st = device_setup(&scratch);
+  if (st != MOE_W4A16_OK) return st;
+  int32_t code = 0;
+  const auto cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&code, scratch, sizeof(code), cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+      cudaStreamSynchronize(cs) != cudaSuccess)
+    return MOE_W4A16_ERR_CUDA;
+  *device_status = static_cast<moe_w4a16_status>(code);
+  return MOE_W4A16_OK;
+}
