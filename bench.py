@@ -318,20 +318,23 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize(dev)
 
     K = args.steps
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(layers)] for _ in range(K)]
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)] if args.graph else None
+    KA = min(K, 200)  # eager steps with events between the calls, after the timed region
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(layers)] for _ in range(KA)]
+    # one event pair per step (nothing between the calls of a step, so the launches of
+    # a step keep their programmatic-dependent-launch overlap)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize(dev)
         t_start.record(stream)
         for i in range(K):
+            sev[i][0].record(stream)
             if args.graph:
-                sev[i][0].record(stream)
                 graphs[i % copies].replay()
-                sev[i][1].record(stream)
             else:
-                step(i, evs[i])
+                step(i)
+            sev[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
@@ -339,16 +342,13 @@ def run_ours(args, rank, world, local):
     if B.moe_w4a16_read_error(buf.workspace, stream) != B.OK:
         raise RuntimeError("a device-side wait timed out during the timed region")
     max_ms = max_over_ranks(elapsed_ms, world, dev)
-    if args.graph:
-        step_ms = np.array([e[0].elapsed_time(e[1]) for e in sev])
-        # the per-call attribution comes from eager steps run after the timed region
-        KA = min(K, 200)
-        for i in range(KA):
-            step(i, evs[i])
-        torch.cuda.synchronize(dev)
-    else:
-        KA = K
-        step_ms = np.array([evs[i][0][0].elapsed_time(evs[i][layers - 1][3]) for i in range(K)])
+    step_ms = np.array([e[0].elapsed_time(e[1]) for e in sev])
+    # the per-call attribution comes from eager steps with events between the calls, run after
+    # the timed region (those events break the launches' overlap, so the parts sum to more
+    # than a timed step)
+    for i in range(KA):
+        step(i, evs[i])
+    torch.cuda.synchronize(dev)
 
     # per-call averages (route, experts, combine)
     parts = np.zeros((layers, 3))
