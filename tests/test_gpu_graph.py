@@ -110,3 +110,41 @@ def test_graph_replay_of_the_sampler(rt):
         for a, b in zip(outs[i], eager[i]):
             assert torch.equal(a, b)
     assert not torch.equal(eager[0][0], eager[1][0])  # another step draws other tokens
+
+
+def test_graph_replay_of_the_moe_block_in_place(rt):
+    """The MoE block (pre-norm, router projection, routing, experts, residual combine) of
+    a two-layer stack captured once, in place (each layer's output overwrites its
+    input), and replayed: equal to the eager calls bit for bit."""
+    wl = synth.WORKLOADS["canvas256"]
+    ws = [synth.make_weights(wl, 0, layer=l) for l in range(2)]
+    dws = [rt.upload_weights(wl, w) for w in ws]
+    gam = [rt.to_device_f32(synth.make_gamma_pre(wl, 0, layer=l)) for l in range(2)]
+    rou = [rt.to_device_u16(synth.make_router(wl, 0, layer=l)) for l in range(2)]
+    buf = rt.alloc_buffers(wl)
+    x0 = [rt.to_device_x(synth.make_x(wl, s)) for s in (21, 22)]
+    xd = x0[0].clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def stack():
+        for l in range(2):
+            rt.run_block(buf, xd, gam[l], rou[l], dws[l], 1e-6, out=xd, stream=s)
+
+    with torch.cuda.stream(s):
+        eager = []
+        for x in x0:
+            xd.copy_(x)
+            stack()
+            eager.append(xd.clone())
+        g = torch.cuda.CUDAGraph()
+        xd.copy_(x0[0])
+        with torch.cuda.graph(g, stream=s):
+            stack()
+        for rep in range(3):
+            xd.copy_(x0[rep % 2])
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(xd.view(torch.int16), eager[rep % 2].view(torch.int16))
+    from w4a16_moe_expert_router_gb300 import binding as B
+    assert B.moe_w4a16_read_error(buf.workspace) == B.OK
