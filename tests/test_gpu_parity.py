@@ -270,3 +270,33 @@ def test_separate_calls_repeated_match_forward(rt, reduction):
     torch.cuda.synchronize()
     assert B.moe_w4a16_read_error(buf.workspace) == B.OK
     assert torch.equal(out, fused)
+
+
+def _fuzz_workload(seed):
+    """A seeded random shape inside the library's range (d % 128, f % 64, groups of
+    32/64/128 dividing d and f, E up to 256, k up to 8), small enough for the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    d = int(rng.choice([128, 256, 384, 512, 768]))
+    f = int(rng.choice([64, 128, 192, 320, 448]))
+    E = int(rng.choice([1, 3, 8, 17, 64, 130, 256]))
+    k = int(rng.integers(1, min(8, E) + 1))
+    T = int(rng.integers(1, 70))
+    g1 = int(rng.choice([g for g in (32, 64, 128) if d % g == 0]))
+    g2 = int(rng.choice([g for g in (32, 64, 128) if f % g == 0]))
+    return synth.Workload(f"fuzz{seed}", T, d, f, E, k, g1, g2, activation=int(rng.integers(0, 2)),
+                          reduction=int(rng.integers(0, 2)), format=int(rng.integers(0, 3)),
+                          zipf_s=float(rng.choice([0.0, 1.1])))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes_against_the_oracle(rt, seed):
+    """Seeded random shapes, formats, reduction orders, activations and routing skews:
+    routing exact, output within the bars, two runs bit-identical."""
+    wl = _fuzz_workload(seed)
+    x, lg, w = synth.make_x(wl, seed), synth.make_logits(wl, seed), synth.make_weights(wl, seed)
+    routing, outs = _gpu_layer(rt, wl, x, lg, w, repeats=2)
+    assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
+    idx, tw = _check_routing(lg, wl.top_k, wl.experts, routing)
+    ref = oracle.forward(x, idx, tw, w, group_gate_up=wl.group_gate_up, group_down=wl.group_down,
+                         activation=wl.activation, nthreads=NCPU, fmt=wl.format)
+    _check_out(outs[0], ref)
