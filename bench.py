@@ -368,35 +368,75 @@ def run_ours(args, rank, world, local):
     achieved = (layer_bytes / layers) / ((route_us if args.block else experts_us) * 1e-6) / 1e9
     layer_gbs = layer_bytes / (ms_per_step * 1e-3) / 1e9
 
-    # end to end through the public API: pinned host buffers, copies inside the timed region
+    # end to end through the public API: every step copies its inputs in from pinned host
+    # memory and its output back, inside the timed region.  The copies in and the copies out
+    # run on two copy streams, double-buffered, so that step i + 1's inputs arrive and step
+    # i - 1's output leaves while step i computes (events order each buffer's reuse).  The host loop makes
+    # the C calls directly (library, and the CUDA runtime for the copies and events) with
+    # argument structures built once, so that it enqueues a step faster than the GPU runs it.
+    rt_lib = ctypes.CDLL("libcudart.so.13")
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    rt_lib.cudaMemcpyAsync.argtypes = [vp, vp, sz, ctypes.c_int, vp]
+    rt_lib.cudaEventRecord.argtypes = [vp, vp]
+    rt_lib.cudaStreamWaitEvent.argtypes = [vp, vp, ctypes.c_uint]
+    rt_lib.cudaEventCreateWithFlags.argtypes = [ctypes.POINTER(vp), ctypes.c_uint]
+    H2D, D2H = 1, 2
+
+    def raw_event():
+        e = vp()
+        if rt_lib.cudaEventCreateWithFlags(ctypes.byref(e), 2) != 0:  # cudaEventDisableTiming
+            raise RuntimeError("cudaEventCreateWithFlags failed")
+        return e
+
+    in_stream, out_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    cptr, optr = in_stream.cuda_stream, out_stream.cuda_stream
     x_host = torch.from_numpy(x_bits.view(np.float16)).pin_memory()
     lg_host = [torch.from_numpy(a).pin_memory() for a in logits]
-    out_host = torch.empty((wl.tokens, wl.hidden), dtype=torch.float16).pin_memory()
-    x_in = torch.empty_like(x)
-    lg_in = [torch.empty_like(a) for a in lg]
+    out_host = [torch.empty((wl.tokens, wl.hidden), dtype=torch.float16).pin_memory() for _ in range(2)]
+    x_in = [torch.empty_like(x) for _ in range(2)]
+    lg_in = [[torch.empty_like(a) for a in lg] for _ in range(2)]
+    out_dev = [torch.empty((wl.tokens, wl.hidden), dtype=torch.float16, device=dev) for _ in range(2)]
+    ev_in = [raw_event() for _ in range(2)]    # the slot's inputs are on the device
+    ev_done = [raw_event() for _ in range(2)]  # the slot's step has finished computing
+    ev_out = [raw_event() for _ in range(2)]   # the slot's output has reached the host
+    used = [False, False]
+    xb, ob = x_host.numel() * 2, wl.tokens * wl.hidden * 2
+    lgb = [a.nbytes for a in logits]
     KE = max(1, min(args.e2e_steps, K))
 
     def e2e_step(i):
-        x_in.copy_(x_host, non_blocking=True)
-        src = x_in
-        if args.block:
+        b = i % 2
+        st = 0
+        if used[b]:
+            st |= rt_lib.cudaStreamWaitEvent(cptr, ev_done[b], 0)  # the step before last has read this slot
+        st |= rt_lib.cudaMemcpyAsync(x_in[b].data_ptr(), x_host.data_ptr(), xb, H2D, cptr)
+        if not args.block:
             for l in range(layers):
-                dst = outs[l % 2]
-                wts = weights[l * copies + (i % copies)]
-                B.moe_w4a16_block(sh, src, gammas_pre[l], 1e-6, routers[l], buf.routing, wts.gate_up, wts.down, dst,
-                                  buf.workspace, stream)
-                src = dst
-            out_host.copy_(src, non_blocking=True)
-            return
+                st |= rt_lib.cudaMemcpyAsync(lg_in[b][l].data_ptr(), lg_host[l].data_ptr(), lgb[l], H2D, cptr)
+        st |= rt_lib.cudaEventRecord(ev_in[b], cptr)
+        st |= rt_lib.cudaStreamWaitEvent(sptr, ev_in[b], 0)
+        if used[b]:
+            st |= rt_lib.cudaStreamWaitEvent(sptr, ev_out[b], 0)  # the step before last's output is out
+        src = x_in[b].data_ptr()
         for l in range(layers):
-            lg_in[l].copy_(lg_host[l], non_blocking=True)
-            dst = outs[l % 2]
-            B.moe_w4a16_route(sh, lg_in[l], buf.routing, buf.workspace, stream)
-            wts = weights[l * copies + (i % copies)]
-            B.moe_w4a16_forward(sh, src, buf.routing, wts.gate_up, wts.down, gammas[l], 1e-6, dst, buf.workspace,
-                                stream)
+            dst = out_dev[b].data_ptr() if l == layers - 1 else outs[l % 2].data_ptr()
+            w_i = l * copies + (i % copies)
+            if args.block:
+                st |= L.moe_w4a16_block(shp, src, gammas_pre[l].data_ptr(), 1e-6, routers[l].data_ptr(), rp,
+                                        ctypes.byref(wstructs[w_i]), dst, ws_ptr, ws_n, sptr)
+            else:
+                g = gammas[l]
+                st |= L.moe_w4a16_route(shp, lg_in[b][l].data_ptr(), rp, ws_ptr, ws_n, sptr)
+                st |= L.moe_w4a16_forward(shp, src, rp, ctypes.byref(wstructs[w_i]),
+                                          None if g is None else g.data_ptr(), 1e-6, dst, ws_ptr, ws_n, sptr)
             src = dst
-        out_host.copy_(src, non_blocking=True)
+        st |= rt_lib.cudaEventRecord(ev_done[b], sptr)
+        st |= rt_lib.cudaStreamWaitEvent(optr, ev_done[b], 0)
+        st |= rt_lib.cudaMemcpyAsync(out_host[b].data_ptr(), out_dev[b].data_ptr(), ob, D2H, optr)
+        st |= rt_lib.cudaEventRecord(ev_out[b], optr)
+        used[b] = True
+        if st:
+            raise RuntimeError(f"a call of the end-to-end step failed with status {st}")
 
     for i in range(min(10, KE)):
         e2e_step(i)
@@ -406,9 +446,14 @@ def run_ours(args, rank, world, local):
     e0.record(stream)
     for i in range(KE):
         e2e_step(i)
+    for b in range(2):
+        rt_lib.cudaStreamWaitEvent(sptr, ev_out[b], 0)  # the last outputs are on the host
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    rt_lib.cudaEventDestroy.argtypes = [vp]
+    for e in ev_in + ev_done + ev_out:
+        rt_lib.cudaEventDestroy(e)
     h2d = x_bits.nbytes + (0 if args.block else sum(a.nbytes for a in logits))
     d2h = wl.tokens * wl.hidden * 2
 
@@ -457,7 +502,10 @@ def run_ours(args, rank, world, local):
             "algorithmic_bytes_per_launch": layer_bytes / layers,
         },
         "e2e": {"value": wl.tokens * KE * world / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE,
+                "copies": "in and out on two copy streams, double-buffered: a step's copies overlap its neighbours' "
+                          "computation; "
+                          "the host loop calls the library and the CUDA runtime directly"},
         # (pre-norm + router projection,) top-k, grouping, row copy, expert GEMMs, combine
         "gpu_launches": K * layers * (6 if args.block else 5),
         "clocks": clocks.summary(),
