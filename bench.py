@@ -633,20 +633,60 @@ def run_sampler(args):
         e1.record()
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    # end to end: pinned host logits in, the four outputs back, every step
+    # end to end: every step copies its logits in from pinned host memory and its four
+    # outputs back, inside the timed region.  The logits go in as four chunks on four copy
+    # streams (several copy engines at once) into one of two device buffers, so that step
+    # i + 1's logits arrive while step i samples; the outputs leave on a stream of their own
+    # from one of two output sets.
     pinned = [torch.from_numpy(h).pin_memory() for h in host]
-    outs_h = [torch.empty(P, dtype=t.dtype, pin_memory=True) for t in (tok, ent, pm, acc)]
+    NC = 4
+    in_streams = [torch.cuda.Stream() for _ in range(NC)]
+    out_stream = torch.cuda.Stream()
+    cur = torch.cuda.current_stream()
+    douts = [[torch.empty(P, dtype=t.dtype, device="cuda") for t in (tok, ent, pm, acc)] for _ in range(2)]
+    outs_h = [[torch.empty(P, dtype=t.dtype, pin_memory=True) for t in (tok, ent, pm, acc)] for _ in range(2)]
+    ev_in = [[torch.cuda.Event() for _ in range(NC)] for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+    n_el = P * V
+    bounds = [n_el * c // NC for c in range(NC + 1)]
+
+    def e2e_call(i):
+        b = i % 2
+        src, dst = pinned[i % 2].view(-1), dev[b].view(-1)
+        for c in range(NC):
+            with torch.cuda.stream(in_streams[c]):
+                if used[b]:
+                    in_streams[c].wait_event(ev_done[b])  # the step before last has read this buffer
+                dst[bounds[c]:bounds[c + 1]].copy_(src[bounds[c]:bounds[c + 1]], non_blocking=True)
+                ev_in[b][c].record(in_streams[c])
+        for c in range(NC):
+            cur.wait_event(ev_in[b][c])
+        if used[b]:
+            cur.wait_event(ev_out[b])  # the step before last's outputs have left this set
+        cfg.step = i
+        B.moe_w4a16_sample(cfg, dev[b], revealed, *douts[b], ws)
+        ev_done[b].record(cur)
+        with torch.cuda.stream(out_stream):
+            out_stream.wait_event(ev_done[b])
+            for o, d in zip(outs_h[b], douts[b]):
+                o.copy_(d, non_blocking=True)
+            ev_out[b].record(out_stream)
+        used[b] = True
+
     e2e_steps = max(3, min(50, steps))
+    for i in range(2):
+        e2e_call(i)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
+    t0.record(cur)
     for i in range(e2e_steps):
-        dev[0].copy_(pinned[i % 2], non_blocking=True)
-        call(i, dev[0])
-        for o, d in zip(outs_h, (tok, ent, pm, acc)):
-            o.copy_(d, non_blocking=True)
-    t1.record()
+        e2e_call(i)
+    for b in range(2):
+        cur.wait_event(ev_out[b])
+    t1.record(cur)
     torch.cuda.synchronize()
     e2e_ms = t0.elapsed_time(t1) / e2e_steps
     bytes_step = P * V * 4
@@ -673,7 +713,9 @@ def run_sampler(args):
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src, "traffic": traffic, "algorithmic_bytes_per_launch": bytes_step},
         "e2e": {"value": 1e3 / e2e_ms, "unit": "steps/s", "h2d_bytes_per_step": bytes_step,
-                "d2h_bytes_per_step": P * (4 + 4 + 4 + 1), "steps": e2e_steps},
+                "d2h_bytes_per_step": P * (4 + 4 + 4 + 1), "steps": e2e_steps,
+                "copies": "logits in as four chunks on four copy streams, double-buffered; outputs out on a "
+                          "stream of their own"},
         "gpu_launches": 2 * steps,
         "clocks": clk.summary(),
     }
