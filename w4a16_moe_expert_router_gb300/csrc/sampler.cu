@@ -77,12 +77,16 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t
                                               const PhiloxKeys& k, uint32_t (&o)[4]) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c0;
-    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
-    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ k.k0[r];
-    const uint32_t n2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ k.k1[r];
-    c1 = static_cast<uint32_t>(p1);
-    c3 = static_cast<uint32_t>(p0);
+    // the two 32 x 32 -> 64-bit products of the round, each one wide multiply
+    uint32_t h0, l0, h1, l1;
+    asm("{\n .reg .u64 t;\n mul.wide.u32 t, %2, %3;\n mov.b64 {%0, %1}, t;\n}" : "=r"(l0), "=r"(h0)
+        : "r"(0xD2511F53u), "r"(c0));
+    asm("{\n .reg .u64 t;\n mul.wide.u32 t, %2, %3;\n mov.b64 {%0, %1}, t;\n}" : "=r"(l1), "=r"(h1)
+        : "r"(0xCD9E8D57u), "r"(c2));
+    const uint32_t n0 = h1 ^ c1 ^ k.k0[r];
+    const uint32_t n2 = h0 ^ c3 ^ k.k1[r];
+    c1 = l1;
+    c3 = l0;
     c0 = n0;
     c2 = n2;
   }
