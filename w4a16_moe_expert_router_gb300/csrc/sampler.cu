@@ -309,7 +309,25 @@ __global__ void __launch_bounds__(kPassThreads, 3)
     __syncthreads();
   }
   int it = 0;
-  for (; it < n_full; ++it) {  // uniform trip count
+  // three iterations per trip over three buffers in turn (cur, nxt, third), each refilled two
+  // iterations ahead, so that no float4 is moved between registers
+  float4 third[2];
+  for (; it + 3 <= n_full; it += 3) {  // uniform trip count
+    const int j = it * kStep + tid;
+    third[0] = load(j + 2 * kStep);
+    third[1] = load(j + 2 * kStep + kPassThreads);
+    pass_iter<false>(S, cur, j, n4, v0, g0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp, &cta_best,
+                     &cta_best);
+    cur[0] = load(j + 3 * kStep);
+    cur[1] = load(j + 3 * kStep + kPassThreads);
+    pass_iter<false>(S, nxt, j + kStep, n4, v0, g0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp, &cta_best,
+                     &cta_best);
+    nxt[0] = load(j + 4 * kStep);
+    nxt[1] = load(j + 4 * kStep + kPassThreads);
+    pass_iter<false>(S, third, j + 2 * kStep, n4, v0, g0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp,
+                     &cta_best, &cta_best);
+  }
+  for (; it < n_full; ++it) {  // the last full iterations, one at a time
     const int j = it * kStep + tid;
     const float4 pf0 = load(j + 2 * kStep), pf1 = load(j + 2 * kStep + kPassThreads);
     pass_iter<false>(S, cur, j, n4, v0, g0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp, &cta_best,
