@@ -225,27 +225,28 @@ __device__ __forceinline__ void pass_iter(PassState& S, const float4 (&x)[2], in
       S.c2 = fminf(fast_exp2(S.m2 - K2 + slack) * 1.01f, 3e38f);
     }
   }
-  bool cand[8];
-  bool any = false;
+  // the largest f + e c2 of the eight: element i is screened in iff its own value is at
+  // least 2 - 2^-23 (implied by w <= e c2, since fl(2 - 2^-24) = 2)
+  float qmax = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    cand[i] = false;
     if (!act[i / 4]) continue;
     const float d = fmaf(l[i], c2e, -S.m2);
     const float e = fast_exp2(d);
     S.z += e;
     S.s1 = fmaf(e, d, S.s1);
-    // with f = 1 + (x & 0x7fffff) 2^-23, w = 1 - U = 2 - 2^-24 - f exactly, so
-    // w <= e c2  <=>  f >= 2 - 2^-24 - e c2, implied by f >= fl(2 - 2^-23 - e c2)
     const float f = __uint_as_float(0x3f800000u | (w[i / 4][i % 4] & 0x007fffffu));
-    cand[i] = f >= fmaf(-e, S.c2, 0x1.fffffep+0f);
-    any |= cand[i];
+    qmax = fmaxf(qmax, fmaf(e, S.c2, f));
   }
+  const bool any = qmax >= 0x1.fffffep+0f;
   if (__any_sync(0xffffffffu, any)) {
     if (any) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        if (!cand[i]) continue;
+        if (!act[i / 4]) continue;
+        const float e = fast_exp2(fmaf(l[i], c2e, -S.m2));
+        const float f = __uint_as_float(0x3f800000u | (w[i / 4][i % 4] & 0x007fffffu));
+        if (!(fmaf(e, S.c2, f) >= 0x1.fffffep+0f)) continue;
         const float k = gumbel_key(l[i], inv_temp, w[i / 4][i % 4]);
         const int32_t v = static_cast<int32_t>(v0 + 4 * static_cast<int64_t>(j + (i / 4) * kPassThreads) + i % 4);
         if (better(k, v, S.bk, S.bv)) {
