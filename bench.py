@@ -724,7 +724,7 @@ def run_sampler(args):
         nth = os.cpu_count() or 1
         sample_p = 32
         t = time.perf_counter()
-        oracle.sample(host[0][:sample_p], 1.0, seed, 0, nthreads=nth)
+        oracle.sample(host[0][:sample_p], 1.0, seed, 0, nthreads=nth, noise=1)
         secs = time.perf_counter() - t
         res["cpu_baseline"] = {"value": 1.0 / (secs * P / sample_p), "unit": "steps/s", "cores": nth,
                                "kind": "oracle", "sample": f"{sample_p} of the {P} positions (fp64 entropy, "
@@ -750,11 +750,11 @@ def run_sampler_reference(args):
     lg = sampler_logits(P, V, copies=1)[0]
     sample_p = max(1, min(P, nth * 2))
     for i in range(min(args.warmup, 1)):
-        oracle.sample(lg[:sample_p], 1.0, seed, i, nthreads=nth)
+        oracle.sample(lg[:sample_p], 1.0, seed, i, nthreads=nth, noise=1)
     budget_s, t0, done, spent = 120.0, time.perf_counter(), 0, 0.0
     for i in range(args.steps):
         t = time.perf_counter()
-        oracle.sample(lg[(i * sample_p) % P:][:sample_p], 1.0, seed, i, nthreads=nth)
+        oracle.sample(lg[(i * sample_p) % P:][:sample_p], 1.0, seed, i, nthreads=nth, noise=1)
         spent += (time.perf_counter() - t) * P / sample_p
         done += 1
         if time.perf_counter() - t0 > budget_s:

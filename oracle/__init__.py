@@ -80,8 +80,18 @@ def lib():
             L.oracle_log_f32.restype = ctypes.c_float
             L.oracle_gumbel_key.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_uint32]
             L.oracle_gumbel_key.restype = ctypes.c_float
+            L.oracle_exp_f32.argtypes = [ctypes.c_float]
+            L.oracle_exp_f32.restype = ctypes.c_float
+            L.oracle_group_counter.argtypes = [ctypes.c_uint32]
+            L.oracle_group_counter.restype = ctypes.c_uint32
+            L.oracle_group_word.argtypes = [ctypes.c_uint32]
+            L.oracle_group_word.restype = ctypes.c_int
+            L.oracle_group_key.argtypes = [vp, ctypes.c_float, ctypes.c_uint32]
+            L.oracle_group_key.restype = ctypes.c_float
+            L.oracle_group_pick.argtypes = [vp, ctypes.c_float, ctypes.c_uint32]
+            L.oracle_group_pick.restype = ctypes.c_int
             L.oracle_sample.argtypes = [i32, i64, vp, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint32,
-                                        ctypes.c_int, vp, vp, vp]
+                                        ctypes.c_int, ctypes.c_int, vp, vp, vp]
             L.oracle_accept_entropy.argtypes = [i32, vp, vp, ctypes.c_float, vp]
             L.oracle_accept_confidence.argtypes = [i32, vp, vp, ctypes.c_float, vp]
             _lib = L
@@ -253,15 +263,39 @@ def gumbel_key(logit: float, inv_temp: float, word: int) -> float:
     return float(lib().oracle_gumbel_key(ctypes.c_float(logit), ctypes.c_float(inv_temp), ctypes.c_uint32(word)))
 
 
-def sample(logits: np.ndarray, inv_temp: float, seed: int, step: int, nthreads: int = 1):
-    """Gumbel-max tokens (int32 [P]) and fp64 entropy and top-1 probability [P] of softmax(logits * inv_temp)."""
+def exp_f32(x: float) -> float:
+    """The fp32 exponential (of x <= 0) the group keys are defined with."""
+    return float(lib().oracle_exp_f32(ctypes.c_float(x)))
+
+
+def group_counter_word(g: int) -> tuple[int, int]:
+    """The Philox counter (first word) and word index of group g (entries 4g .. 4g+3)."""
+    return int(lib().oracle_group_counter(int(g))), int(lib().oracle_group_word(int(g)))
+
+
+def group_key(l4, inv_temp: float, word: int) -> float:
+    """Gumbel key of a group of four logits under one Philox word."""
+    a = _c(l4, np.float32)
+    return float(lib().oracle_group_key(_ptr(a), ctypes.c_float(inv_temp), ctypes.c_uint32(word)))
+
+
+def group_pick(l4, inv_temp: float, word: int) -> int:
+    """The token (0 .. 3) inside a group of four logits under one Philox word."""
+    a = _c(l4, np.float32)
+    return int(lib().oracle_group_pick(_ptr(a), ctypes.c_float(inv_temp), ctypes.c_uint32(word)))
+
+
+def sample(logits: np.ndarray, inv_temp: float, seed: int, step: int, nthreads: int = 1, noise: int = 0):
+    """Gumbel-max tokens (int32 [P]) and fp64 entropy and top-1 probability [P] of
+    softmax(logits * inv_temp); noise 0 draws one Gumbel per group of four entries,
+    1 one per entry."""
     lg = _c(logits, np.float32)
     P, V = lg.shape
     tok = np.zeros(P, np.int32)
     ent = np.zeros(P, np.float64)
     pm = np.zeros(P, np.float64)
-    st = lib().oracle_sample(P, V, _ptr(lg), float(inv_temp), int(seed), int(step), int(nthreads), _ptr(tok),
-                             _ptr(ent), _ptr(pm))
+    st = lib().oracle_sample(P, V, _ptr(lg), float(inv_temp), int(seed), int(step), int(noise), int(nthreads),
+                             _ptr(tok), _ptr(ent), _ptr(pm))
     if st != OK:
         raise ValueError(f"oracle_sample status {st}")
     return tok, ent, pm

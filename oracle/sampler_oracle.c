@@ -27,14 +27,33 @@
  *   - the sampled distribution is softmax(t), t_v = logit_v * inv_temp, and the
  *     entropy is that distribution's, H = -sum_v p_v ln p_v (natural log); the
  *     confidence of a position is max_v p_v;
- *   - Gumbel-max: token = argmax_v (t_v + G_v), G_v = -ln(-ln U_v), ties to the lower
- *     index; U_v = ((x & 0x7fffff) + 1/2) 2^-23 from the low 23 bits of the 32-bit
- *     word x that Philox4x32-10
- *     gives for element v: counter (v / 4, position, step, 0), key (seed low, seed
- *     high), word v % 4;
- *   - the key t_v + G_v decides an integer, so it is defined in fp32 with one IEEE
- *     rounding per operation (log_f32 below, then fmaf(logit, inv_temp, G)); any
- *     implementation that follows these steps gets the same bits;
+ *   - Gumbel-max, two forms selected by `noise` (both sample softmax(t) exactly in
+ *     real arithmetic; [MC] fixes the distribution and the Gumbel-max method, not how
+ *     the noise is laid over the vocabulary):
+ *     noise 1 (one Gumbel per token): token = argmax_v (t_v + G_v), G_v = -ln(-ln U_v),
+ *       ties to the lower index; U_v = ((x & 0x7fffff) + 1/2) 2^-23 from the low 23
+ *       bits of the 32-bit word x that Philox4x32-10 gives for element v: counter
+ *       (v / 4, position, step, 0), key (seed low, seed high), word v % 4;
+ *     noise 0 (one Gumbel per group of four, the default): the vocabulary is cut into
+ *       groups g of four consecutive entries (4g .. 4g+3).  The largest of four
+ *       independent Gumbel keys t_i + G_i is itself Gumbel-distributed around
+ *       LSE_g = ln sum_i e^(t_i), and which of the four attains it is independent of
+ *       that value and distributed as softmax over the group (the max-stability of the
+ *       Gumbel law, the top-down construction of a Gumbel process).  So the group's
+ *       key is LSE_g + G_g with one Gumbel G_g, the token's group is the argmax of
+ *       the group keys (ties to the lower group), and the token inside it is drawn by
+ *       inverse CDF from a second uniform U'_g: the first i whose running sum of
+ *       e^(t_i - m) exceeds U'_g times the group's sum.  U_g comes from Philox word
+ *       r / 256 of counter (256 (g / 1024) + r % 256, position, step, 0), r = g % 1024
+ *       (the 1,024 groups of each 4,096-entry block share 256 counters), and U'_g from
+ *       the same word of the counter with fourth word 1.  This mapping was chosen to
+ *       suit the GPU pass, whose threads own float4s 256 apart; any bijection would do;
+ *   - each key decides an integer, so it is defined in fp32 with one IEEE rounding per
+ *     operation (log_f32 and exp_f32 below; the per-token key is
+ *     fmaf(logit, inv_temp, G), the group key fl(fl(m + ln S) + G) with
+ *     t_i = fl(l_i inv_temp), m = max t_i, S = ((e_0 + e_1) + e_2) + e_3,
+ *     e_i = exp_f32(fl(t_i - m))); any implementation that follows these steps gets
+ *     the same bits;
  *   - both acceptance rules consider only positions not yet revealed; the
  *     entropy-bound rule evaluates the mlx-vlm formula elementwise in fp32 over the
  *     sorted entropies (ties: lower position first).
@@ -129,6 +148,83 @@ float oracle_gumbel_key(float logit, float inv_temp, uint32_t word) {
   return fmaf(logit, inv_temp, g);
 }
 
+/* --------------------------------------------------------- fp32 exp ---- */
+
+/* e^x for x <= 0, defined as a sequence of IEEE fp32 operations:
+ *   below -87 (where 2^n would leave the normal range) the result is 0;
+ *   n = rint(fl(x * LOG2E)), LOG2E = fp32 log2(e) = 0x1.715476p+0;
+ *   r = fmaf(-n, LN2_LO, fmaf(-n, LN2_HI, x))  (the split of ln 2 used by log_f32);
+ *   P = 1 + r(1 + r(1/2 + r(1/6 + r(1/24 + r(1/120 + r(1/720 + r/5040))))))
+ *       (the Taylor series of e^r to r^7, Horner with fmaf, coefficients the fp32
+ *       quotients 1.0f / 5040.0f, ...; |r| <= 0.35, so the first omitted term is below
+ *       2^-27 of the result);
+ *   e^x = fl(P * 2^n), 2^n built from its exponent bits. */
+float oracle_exp_f32(float x) {
+  if (!(x >= -87.0f)) return 0.0f;
+  const float n = rintf(x * 0x1.715476p+0f);
+  float r = fmaf(-n, 0.693145751953125f, x);
+  r = fmaf(-n, 1.42860677e-06f, r);
+  float p = 1.0f / 5040.0f;
+  p = fmaf(p, r, 1.0f / 720.0f);
+  p = fmaf(p, r, 1.0f / 120.0f);
+  p = fmaf(p, r, 1.0f / 24.0f);
+  p = fmaf(p, r, 1.0f / 6.0f);
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  const uint32_t sb = (uint32_t)((int)n + 127) << 23;
+  float sc;
+  memcpy(&sc, &sb, 4);
+  return p * sc;
+}
+
+/* ------------------------------------------------- groups of four ---- */
+
+/* The Philox counter (first word) and the word index of group g. */
+uint32_t oracle_group_counter(uint32_t g) { return ((g >> 10) << 8) | (g & 255u); }
+int oracle_group_word(uint32_t g) { return (int)((g >> 8) & 3u); }
+
+/* t_i = fl(l_i inv_temp), m = max t_i, e_i = exp_f32(fl(t_i - m)), S = ((e_0 + e_1) + e_2) + e_3. */
+static float group_exp(const float* l, float inv_temp, float* e) {
+  float t[4];
+  for (int i = 0; i < 4; ++i) t[i] = l[i] * inv_temp;
+  const float m = fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
+  for (int i = 0; i < 4; ++i) e[i] = oracle_exp_f32(t[i] - m);
+  return m;
+}
+
+/* The key of a group of four logits: LSE = fl(m + ln S), G = -ln(-ln U) from the
+ * word's low 23 bits, key = fl(LSE + G). */
+float oracle_group_key(const float* l, float inv_temp, uint32_t word) {
+  float e[4];
+  const float m = group_exp(l, inv_temp, e);
+  const float S = ((e[0] + e[1]) + e[2]) + e[3];
+  const float lse = m + oracle_log_f32(S);
+  const float u = ((float)(word & 0x007fffffu) + 0.5f) * 0x1p-23f;
+  const float g = -oracle_log_f32(-oracle_log_f32(u));
+  return lse + g;
+}
+
+/* The token inside a group (0 .. 3) by inverse CDF: U' from the word's low 23 bits,
+ * T = fl(U' S); the first i with fl(..fl(e_0 + e_1).. + e_i) > T; if none (T rounded up
+ * to S), the last i with e_i > 0. */
+int oracle_group_pick(const float* l, float inv_temp, uint32_t word) {
+  float e[4];
+  group_exp(l, inv_temp, e);
+  const float S = ((e[0] + e[1]) + e[2]) + e[3];
+  const float u = ((float)(word & 0x007fffffu) + 0.5f) * 0x1p-23f;
+  const float T = u * S;
+  float c = 0.0f;
+  for (int i = 0; i < 4; ++i) {
+    c = i == 0 ? e[0] : c + e[i];
+    if (c > T) return i;
+  }
+  int last = 0;
+  for (int i = 0; i < 4; ++i)
+    if (e[i] > 0.0f) last = i;
+  return last;
+}
+
 /* ---------------------------------------------------------- sampling ---- */
 
 typedef struct {
@@ -138,14 +234,15 @@ typedef struct {
   float inv_temp;
   uint32_t key[2];
   uint32_t step;
+  int noise;
   int32_t* token;
   double* entropy;
   double* pmax;
 } sample_job;
 
 /* Positions [p0, p1): the fp64 entropy and top-1 probability of softmax(t), and the
- * Gumbel-max token (element by element in vocabulary order, a strictly larger key
- * replaces the best, so ties keep the lower index). */
+ * Gumbel-max token (keys in vocabulary order, per token or per group; a strictly larger
+ * key replaces the best, so ties keep the lower index). */
 static void* sample_worker(void* arg) {
   const sample_job* j = (const sample_job*)arg;
   for (int p = j->p0; p < j->p1; ++p) {
@@ -166,29 +263,49 @@ static void* sample_worker(void* arg) {
     j->pmax[p] = 1.0 / Z;
     float best = -INFINITY;
     int32_t tok = 0;
-    for (int64_t g = 0; g < j->V / 4; ++g) {
-      const uint32_t ctr[4] = {(uint32_t)g, (uint32_t)p, j->step, 0u};
-      uint32_t words[4];
-      oracle_philox4x32_10(ctr, j->key, words);
-      for (int i = 0; i < 4; ++i) {
-        const int64_t v = 4 * g + i;
-        const float k = oracle_gumbel_key(l[v], j->inv_temp, words[i]);
-        if (k > best) {
-          best = k;
-          tok = (int32_t)v;
+    if (j->noise == 1) {
+      for (int64_t g = 0; g < j->V / 4; ++g) {
+        const uint32_t ctr[4] = {(uint32_t)g, (uint32_t)p, j->step, 0u};
+        uint32_t words[4];
+        oracle_philox4x32_10(ctr, j->key, words);
+        for (int i = 0; i < 4; ++i) {
+          const int64_t v = 4 * g + i;
+          const float k = oracle_gumbel_key(l[v], j->inv_temp, words[i]);
+          if (k > best) {
+            best = k;
+            tok = (int32_t)v;
+          }
         }
       }
+    } else {
+      uint32_t bg = 0;
+      for (int64_t g = 0; g < j->V / 4; ++g) {
+        const uint32_t ctr[4] = {oracle_group_counter((uint32_t)g), (uint32_t)p, j->step, 0u};
+        uint32_t words[4];
+        oracle_philox4x32_10(ctr, j->key, words);
+        const float k = oracle_group_key(l + 4 * g, j->inv_temp, words[oracle_group_word((uint32_t)g)]);
+        if (k > best) {
+          best = k;
+          bg = (uint32_t)g;
+        }
+      }
+      const uint32_t ctr[4] = {oracle_group_counter(bg), (uint32_t)p, j->step, 1u};
+      uint32_t words[4];
+      oracle_philox4x32_10(ctr, j->key, words);
+      tok = (int32_t)(4 * bg) + oracle_group_pick(l + 4 * (int64_t)bg, j->inv_temp, words[oracle_group_word(bg)]);
     }
     j->token[p] = tok;
   }
   return NULL;
 }
 
-/* logits fp32 [P][V] (V a multiple of 4, all finite), inv_temp > 0 and finite.
+/* logits fp32 [P][V] (V a multiple of 4, all finite), inv_temp > 0 and finite,
+ * noise 0 (one Gumbel per group of four) or 1 (one per token).
  * Outputs token [P], entropy [P] and pmax [P] (fp64). */
 int oracle_sample(int P, int64_t V, const float* logits, float inv_temp, uint64_t seed, uint32_t step,
-                  int nthreads, int32_t* token, double* entropy, double* pmax) {
+                  int noise, int nthreads, int32_t* token, double* entropy, double* pmax) {
   if (P < 1 || V < 4 || V % 4 != 0 || V > ((int64_t)1 << 32)) return SAMPLER_ERR_SHAPE;
+  if (noise != 0 && noise != 1) return SAMPLER_ERR_SHAPE;
   if (!(inv_temp > 0.0f) || !isfinite(inv_temp)) return SAMPLER_ERR_SHAPE;
   for (int64_t i = 0; i < (int64_t)P * V; ++i)
     if (!isfinite(logits[i])) return SAMPLER_ERR_NONFINITE;
@@ -211,6 +328,7 @@ int oracle_sample(int P, int64_t V, const float* logits, float inv_temp, uint64_
     j->key[0] = (uint32_t)seed;
     j->key[1] = (uint32_t)(seed >> 32);
     j->step = step;
+    j->noise = noise;
     j->token = token;
     j->entropy = entropy;
     j->pmax = pmax;

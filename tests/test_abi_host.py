@@ -361,7 +361,7 @@ def test_smoke_sampler_check_with_a_host_stand_in():
 
     def fake_sample(cfg, logits, revealed, token, entropy, pmax, accept, workspace, stream=None):
         lg = logits.cpu().numpy()
-        t, e, pm = oracle.sample(lg, cfg.inv_temperature, cfg.seed, cfg.step)
+        t, e, pm = oracle.sample(lg, cfg.inv_temperature, cfg.seed, cfg.step, noise=1)
         token.copy_(torch.from_numpy(t))
         entropy.copy_(torch.from_numpy(e.astype(np.float32)))
         pmax.copy_(torch.from_numpy(pm.astype(np.float32)))

@@ -63,7 +63,7 @@ def _gpu_sample(B, lg, revealed, inv_temp, rule, bound, seed, step, repeats=1):
 
 def _check(lg, revealed, inv_temp, rule, bound, seed, step, got):
     tok, ent, pm, acc = got
-    o_tok, o_ent, o_pm = oracle.sample(lg, inv_temp, seed, step, nthreads=NCPU)
+    o_tok, o_ent, o_pm = oracle.sample(lg, inv_temp, seed, step, nthreads=NCPU, noise=1)
     assert np.array_equal(tok, o_tok), np.nonzero(tok != o_tok)[0][:10]
     assert np.all(np.abs(ent.astype(np.float64) - o_ent) <= 2e-5 + 2e-5 * np.abs(o_ent)), \
         float(np.abs(ent - o_ent).max())

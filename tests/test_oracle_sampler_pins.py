@@ -1,15 +1,16 @@
 """Pins of the sampler oracle (oracle/sampler_oracle.c) to things other than itself:
-libm's logarithm, closed forms of the entropy, the distribution Gumbel-max must
-sample, generator statistics, and the page's own formula of the entropy-bound rule.
+libm's logarithm and exponential, closed forms of the entropy and of the group keys,
+the distribution Gumbel-max must sample (per token and per group of four), the
+generator's published known-answer vectors and statistics, and the page's own
+formula of the entropy-bound rule.
 
 Sources: "srswti/axe-diffusion-ksl-xe" model card ("the kernels we built": entropy in
 one streaming pass, Gumbel-max instead of softmax + multinomial); "lablup/mlxcel
 block-diffusion docs" ("Samplers": the entropy-bound rule, the mlx-vlm formula
 (cumsum - cummax) <= bound, at least one accepted; the confidence-threshold rule);
-Salmon et al., SC'11 (Philox4x32-10).
-
-The bit pattern of Philox4x32-10 itself is pinned only by statistics here and by the
-bit-exact agreement of the GPU path's independent implementation with this one.
+Salmon et al., SC'11 (Philox4x32-10); the max-stability of the Gumbel law (the maximum
+of independent Gumbel(mu_i) variables is Gumbel(ln sum_i e^mu_i), attained at i with
+probability proportional to e^mu_i), which the per-group form rests on.
 """
 import math
 
@@ -146,18 +147,47 @@ def test_temperature_scales_the_logits():
 
 # ------------------------------------------------------------------ Gumbel-max
 
+@pytest.mark.parametrize("noise", [0, 1])
 @pytest.mark.parametrize("inv_temp", [1.0, 0.5])
-def test_gumbel_max_samples_the_softmax(inv_temp):
+def test_gumbel_max_samples_the_softmax(inv_temp, noise):
     """The tokens of 40000 positions with the same logits (each position its own
-    counters) follow softmax(logits * inv_temp): chi-square at p = 1e-4."""
+    counters) follow softmax(logits * inv_temp): chi-square at p = 1e-4.  Per group,
+    a wrong group sum, a missing ln S, a pick from the wrong end of the CDF or a group's
+    noise taken from another group's word skews it far past the bound."""
     base = np.array([0.0, 1.0, 2.0, -1.0, 0.5, 3.0, -2.0, 1.5], np.float32)
     P = 40000
-    tok, _, _ = oracle.sample(np.tile(base, (P, 1)), inv_temp, 11, 4, nthreads=8)
+    tok, _, _ = oracle.sample(np.tile(base, (P, 1)), inv_temp, 11, 4, nthreads=8, noise=noise)
     p = np.exp(base.astype(np.float64) * inv_temp)
     p /= p.sum()
     counts = np.bincount(tok, minlength=8)
     chi2 = float(((counts - P * p) ** 2 / (P * p)).sum())
     assert chi2 < 29.9  # chi-square, 7 degrees of freedom, p = 1e-4
+
+
+def test_grouped_gumbel_max_over_many_groups():
+    """24 entries (six groups, one of them far ahead, one far behind) over 30000
+    positions and two steps: the per-group form samples softmax, chi-square at
+    p = 1e-4 over the entries with an expected count of at least 5."""
+    rng = np.random.default_rng(12)
+    base = rng.normal(0.0, 1.5, 24).astype(np.float32)
+    base[8:12] += 2.5
+    base[16:20] -= 4.0
+    P = 30000
+    p = np.exp(base.astype(np.float64))
+    p /= p.sum()
+    counts = np.zeros(24)
+    for step in (0, 1):
+        tok, _, _ = oracle.sample(np.tile(base, (P, 1)), 1.0, 99, step, nthreads=8, noise=0)
+        counts += np.bincount(tok, minlength=24)
+    n = 2 * P
+    keep = n * p >= 5
+    other = counts[~keep].sum(), n * p[~keep].sum()
+    chi2 = float(((counts[keep] - n * p[keep]) ** 2 / (n * p[keep])).sum())
+    if other[1] > 0:
+        chi2 += (other[0] - other[1]) ** 2 / other[1]
+    dof = int(keep.sum()) - (0 if other[1] > 0 else 1)
+    scipy_stats = pytest.importorskip("scipy.stats")
+    assert chi2 < scipy_stats.chi2.ppf(1 - 1e-4, dof), (chi2, dof)
 
 
 def test_gumbel_key_matches_the_definition_in_fp64():
@@ -172,18 +202,118 @@ def test_gumbel_key_matches_the_definition_in_fp64():
         assert abs(got - want) <= 8 * _ulp(want) + 1e-6
 
 
-def test_dominant_logit_wins_and_seeds_change_draws():
+@pytest.mark.parametrize("noise", [0, 1])
+def test_dominant_logit_wins_and_seeds_change_draws(noise):
     lg = np.zeros((4, 256), np.float32)
     lg[:, 77] = 60.0  # exp(60) outweighs any Gumbel noise the 23-bit uniforms can give (G <= 16.7)
-    tok, _, _ = oracle.sample(lg, 1.0, 5, 9)
+    tok, _, _ = oracle.sample(lg, 1.0, 5, 9, noise=noise)
     assert np.all(tok == 77)
     rng = np.random.default_rng(4)
     lg = rng.standard_normal((64, 1024)).astype(np.float32)
-    t1, _, _ = oracle.sample(lg, 1.0, 1, 0)
-    t2, _, _ = oracle.sample(lg, 1.0, 2, 0)
-    t3, _, _ = oracle.sample(lg, 1.0, 1, 1)
-    assert np.array_equal(t1, oracle.sample(lg, 1.0, 1, 0)[0])
+    t1, _, _ = oracle.sample(lg, 1.0, 1, 0, noise=noise)
+    t2, _, _ = oracle.sample(lg, 1.0, 2, 0, noise=noise)
+    t3, _, _ = oracle.sample(lg, 1.0, 1, 1, noise=noise)
+    assert np.array_equal(t1, oracle.sample(lg, 1.0, 1, 0, noise=noise)[0])
     assert (t1 != t2).mean() > 0.5 and (t1 != t3).mean() > 0.5
+
+
+# ------------------------------------------------------------------ groups of four
+
+def test_exp_f32_against_libm():
+    """Within 1 fp32 ulp of the exact exponential over [-87, 0] (measured worst 0.9),
+    exactly 1 at 0 and 0 below -87; dropping the r^7 term costs 2.5 ulps, dropping the
+    low part of ln 2 thousands, a wrong coefficient more."""
+    rng = np.random.default_rng(8)
+    xs = np.concatenate([-rng.uniform(0, 87, 60000), -np.arange(0, 2000) * 2.0 ** -20,
+                         -87 + np.arange(0, 2000) * 1e-4, -(2.0 ** rng.uniform(-40, 6.4, 20000))]).astype(np.float32)
+    worst = 0.0
+    prev = None
+    for x in np.sort(xs)[::3]:
+        got = oracle.exp_f32(float(x))
+        want = math.exp(float(x))
+        worst = max(worst, abs(got - want) / _ulp(want))
+        if prev is not None:
+            assert got >= prev  # monotone on the sorted grid
+        prev = got
+    assert worst <= 1.0, worst
+    assert oracle.exp_f32(0.0) == 1.0 and oracle.exp_f32(-0.0) == 1.0
+    assert oracle.exp_f32(-87.0001) == 0.0 and oracle.exp_f32(-1000.0) == 0.0
+
+
+def test_group_counter_word_is_a_bijection_onto_the_blocks_counters():
+    """Every (counter, word) pair is used by exactly one group, and the groups of
+    4,096-entry block b use exactly counters 256 b .. 256 b + 255."""
+    G = 1024 * 5
+    pairs = [oracle.group_counter_word(g) for g in range(G)]
+    assert len(set(pairs)) == G
+    for b in range(5):
+        cs = {c for c, _ in pairs[1024 * b:1024 * (b + 1)]}
+        assert cs == set(range(256 * b, 256 * b + 256))
+    assert {w for _, w in pairs} == {0, 1, 2, 3}
+
+
+def _g_of(word: int) -> float:
+    u = ((word & 0x7FFFFF) + 0.5) * 2.0 ** -23
+    return -math.log(-math.log(u))
+
+
+def test_group_key_closed_forms():
+    """Four equal logits: key = a + ln 4 + G.  One logit far ahead of the others
+    (their e^(t - m) underflows to 0): the key is that entry's per-token key, bit for
+    bit (inv_temp 1, so both are fl(a + G)).  Random groups: key - G = ln sum e^t
+    within fp32 rounding (a dropped term of the sum, a missing ln or a max taken
+    wrongly all fail)."""
+    rng = np.random.default_rng(9)
+    for w in rng.integers(0, 2 ** 32, 300, dtype=np.uint64):
+        w = int(w)
+        a = float(np.float32(rng.uniform(-20, 20)))
+        got = oracle.group_key([a] * 4, 1.0, w)
+        want = a + math.log(4.0) + _g_of(w)
+        assert abs(got - want) <= 8 * _ulp(want) + 1e-6
+        l4 = np.full(4, a - 200.0, np.float32)
+        i = int(rng.integers(0, 4))
+        l4[i] = a
+        assert oracle.group_key(l4, 1.0, w) == oracle.gumbel_key(a, 1.0, w)
+        l4 = rng.normal(0, 3, 4).astype(np.float32)
+        it = float(np.float32(rng.uniform(0.3, 2.0)))
+        t = l4.astype(np.float64) * it
+        want = float(np.log(np.exp(t).sum())) + _g_of(w)
+        got = oracle.group_key(l4, it, w)
+        assert abs(got - want) <= 16 * _ulp(want) + 2e-6, (got, want)
+
+
+def test_group_pick_is_the_inverse_cdf():
+    """Logits ln 1 .. ln 4 give probabilities 0.1 .. 0.4: the pick is the first i whose
+    cumulative probability exceeds U' (checked away from the boundaries); equal logits
+    give floor(4 U'); a dominant entry is always picked."""
+    rng = np.random.default_rng(10)
+    l4 = np.log(np.array([1.0, 2.0, 3.0, 4.0])).astype(np.float32)
+    cdf = np.array([0.1, 0.3, 0.6, 1.0])
+    seen = set()
+    for w in rng.integers(0, 2 ** 32, 3000, dtype=np.uint64):
+        w = int(w)
+        u = ((w & 0x7FFFFF) + 0.5) * 2.0 ** -23
+        if np.min(np.abs(cdf - u)) < 1e-5 or min(abs(u - k / 4) for k in range(5)) < 1e-5:
+            continue
+        want = int(np.argmax(cdf > u))
+        assert oracle.group_pick(l4, 1.0, w) == want
+        assert oracle.group_pick([1.5] * 4, 1.0, w) == int(4 * u)
+        seen.add(want)
+        assert oracle.group_pick([-3.0, 9.0, -80.0, -3.0], 1.0, w) == 1
+    assert seen == {0, 1, 2, 3}
+
+
+def test_one_group_vocabulary_is_the_pick_of_its_second_stream():
+    """V = 4: the group wins trivially, so the token is the inverse-CDF pick under word 0
+    of counter (0, position, step, 1) of the published generator."""
+    rng = np.random.default_rng(11)
+    lg = rng.normal(0, 1, (200, 4)).astype(np.float32)
+    seed, step = 0x0123_4567_89AB_CDEF, 7
+    tok, _, _ = oracle.sample(lg, 0.8, seed, step, noise=0)
+    key = np.array([seed & 0xFFFFFFFF, seed >> 32], np.uint32)
+    for p in range(200):
+        w = oracle.philox4x32_10([0, p, step, 1], key)[0]
+        assert tok[p] == oracle.group_pick(lg[p], 0.8, int(w))
 
 
 # ------------------------------------------------------------------ acceptance
