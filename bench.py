@@ -61,6 +61,8 @@ def parse_args(argv=None):
                    help="replay each step from a CUDA graph captured once (per weight copy) instead of launching it")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--sampler", action="store_true", help="time the per-step sampler instead of the layer")
+    p.add_argument("--noise", type=int, choices=[0, 1], default=0,
+                   help="sampler Gumbel noise: 0 one Gumbel per group of four entries, 1 one per token")
     p.add_argument("--block", action="store_true",
                    help="time the whole MoE block per layer (pre-norm, router projection, routing, experts, "
                         "combine with the residual) as one moe_w4a16_block call; logits are not an input")
@@ -615,7 +617,7 @@ def run_sampler(args):
     ent = torch.empty(P, dtype=torch.float32, device="cuda")
     pm = torch.empty(P, dtype=torch.float32, device="cuda")
     acc = torch.empty(P, dtype=torch.uint8, device="cuda")
-    cfg = B.make_sampler(P, V, 1.0, 0, 40.0, 0, seed)
+    cfg = B.make_sampler(P, V, 1.0, 0, 40.0, 0, seed, args.noise)
     ws = torch.empty(B.moe_w4a16_sampler_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
 
     def call(i, lg):
@@ -696,7 +698,7 @@ def run_sampler(args):
     if os.path.exists(SAMPLER_PROFILE):
         vals = dict(ln.split(":", 1) for ln in open(SAMPLER_PROFILE) if ":" in ln)
         vals = {k.strip(): v.strip() for k, v in vals.items()}
-        if vals.get("kernel_source_sha256_16") == source_hash(SAMPLER_SRC):
+        if vals.get("kernel_source_sha256_16") == source_hash(SAMPLER_SRC) and vals.get("noise") == str(args.noise):
             try:
                 traffic = float(vals["traffic_bytes_per_launch_full_size"])
             except (KeyError, ValueError):
@@ -706,8 +708,8 @@ def run_sampler(args):
         "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": "sampler_p256_v262144", "positions": P, "vocab": V, "logits": "3 * N(0, 1) fp32",
-                   "rule": "entropy bound 40", "l2": "inputs larger than L2: 268 MB of logits per step vs 129 MB "
-                                                    "L2; two copies alternate"},
+                   "rule": "entropy bound 40", "noise": NOISE_NAMES[args.noise],
+                   "l2": "inputs larger than L2: 268 MB of logits per step vs 129 MB L2; two copies alternate"},
         "roofline": {"kernel": "sample_pass_kernel + sample_final_kernel (the whole call: one streaming pass over "
                                "the logits, then one CTA merging the partials and deciding the acceptance)",
                      "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -724,13 +726,16 @@ def run_sampler(args):
         nth = os.cpu_count() or 1
         sample_p = 32
         t = time.perf_counter()
-        oracle.sample(host[0][:sample_p], 1.0, seed, 0, nthreads=nth, noise=1)
+        oracle.sample(host[0][:sample_p], 1.0, seed, 0, nthreads=nth, noise=args.noise)
         secs = time.perf_counter() - t
+        keys = f"Gumbel keys of all {V // 4} groups" if args.noise == 0 else f"Gumbel keys of all {V} tokens"
         res["cpu_baseline"] = {"value": 1.0 / (secs * P / sample_p), "unit": "steps/s", "cores": nth,
                                "kind": "oracle", "sample": f"{sample_p} of the {P} positions (fp64 entropy, "
-                                                           f"Gumbel keys of all {V} tokens), {nth} threads, "
-                                                           "scaled to a full step"}
+                                                           f"{keys}), {nth} threads, scaled to a full step"}
     return res
+
+
+NOISE_NAMES = {0: "one Gumbel per group of four entries", 1: "one Gumbel per token"}
 
 
 def sampler_logits(P, V, copies=2):
@@ -750,11 +755,11 @@ def run_sampler_reference(args):
     lg = sampler_logits(P, V, copies=1)[0]
     sample_p = max(1, min(P, nth * 2))
     for i in range(min(args.warmup, 1)):
-        oracle.sample(lg[:sample_p], 1.0, seed, i, nthreads=nth, noise=1)
+        oracle.sample(lg[:sample_p], 1.0, seed, i, nthreads=nth, noise=args.noise)
     budget_s, t0, done, spent = 120.0, time.perf_counter(), 0, 0.0
     for i in range(args.steps):
         t = time.perf_counter()
-        oracle.sample(lg[(i * sample_p) % P:][:sample_p], 1.0, seed, i, nthreads=nth, noise=1)
+        oracle.sample(lg[(i * sample_p) % P:][:sample_p], 1.0, seed, i, nthreads=nth, noise=args.noise)
         spent += (time.perf_counter() - t) * P / sample_p
         done += 1
         if time.perf_counter() - t0 > budget_s:
@@ -765,7 +770,7 @@ def run_sampler_reference(args):
         "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 * spent / done, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "sampler_p256_v262144", "positions": P, "vocab": V, "logits": "3 * N(0, 1) fp32",
-                   "rule": "entropy bound 40"},
+                   "rule": "entropy bound 40", "noise": NOISE_NAMES[args.noise]},
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": nth, "kind": "oracle",
                          "sample": f"{sample_p} of the {P} positions per step, {nth} threads, scaled to a full step"},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

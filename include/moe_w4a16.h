@@ -248,13 +248,27 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_block(const moe_w4a16_shape* shape, con
  * the two acceptance rules).  Per position p, with t_v = logits[p][v] * inv_temperature:
  *   entropy[p]  H = -sum_v q_v ln q_v of q = softmax(t)                    (fp32)
  *   pmax[p]     max_v q_v                                                  (fp32)
- *   token[p]    argmax_v (t_v + G_v), ties to the lower v; G_v = -ln(-ln U_v),
- *               U_v = ((x & 0x7fffff) + 1/2) 2^-23, x = word v % 4 of Philox4x32-10
- *               (Salmon et al., SC'11) at counter (v / 4, p, step, 0) under key
- *               (seed & 0xffffffff, seed >> 32); the key is evaluated in fp32 with
- *               one IEEE rounding per step (the natural log as range reduction plus
- *               the atanh series to s^11, then fma(logit, inv_temperature, G)), so
- *               the token is reproducible bit for bit off the GPU
+ *   token[p]    a Gumbel-max draw from q, in one of two forms (cfg.noise):
+ *               noise 0 (one Gumbel per group of four, the default): group g holds
+ *                 entries 4g .. 4g+3; its key is fl(fl(m + ln S) + G_g) with
+ *                 t_i = fl(l_i inv_temperature), m = max t_i, e_i = exp(fl(t_i - m)),
+ *                 S = ((e_0 + e_1) + e_2) + e_3, G_g = -ln(-ln U_g); the winning group
+ *                 is the argmax (ties to the lower g) and the token inside it the
+ *                 first i with fl(..fl(e_0 + e_1).. + e_i) > fl(U'_g S) (if none, the
+ *                 last i with e_i > 0).  U_g / U'_g come from word r / 256, r = g % 1024,
+ *                 of Philox4x32-10 at counter (256 (g / 1024) + r % 256, p, step, 0 / 1).
+ *                 The maximum of the four per-token keys below is Gumbel around
+ *                 ln sum_i e^(t_i) and falls on i with probability proportional to e^(t_i)
+ *                 (max-stability of the Gumbel law), so both forms sample q;
+ *               noise 1 (one Gumbel per token): argmax_v (t_v + G_v), ties to the lower
+ *                 v; G_v = -ln(-ln U_v), U_v from word v % 4 of Philox4x32-10 at
+ *                 counter (v / 4, p, step, 0), key fma(logit, inv_temperature, G_v).
+ *               U = ((x & 0x7fffff) + 1/2) 2^-23 of a word x; Philox4x32-10 (Salmon et
+ *               al., SC'11) under key (seed & 0xffffffff, seed >> 32).  Every key is
+ *               evaluated in fp32 with one IEEE rounding per step (the natural log as
+ *               range reduction plus the atanh series to s^11, the exponential as range
+ *               reduction plus the Taylor series to r^7, 0 below -87), so the token is
+ *               reproducible bit for bit off the GPU
  *   accept[p]   rule 0 (entropy bound): among positions with revealed[p] == 0,
  *               sorted by (entropy, p), sorted position i is accepted iff
  *               fl(c_i - x_i) <= bound, c_i / x_i the fp32 running sum / maximum of
@@ -271,6 +285,7 @@ typedef struct {
   int32_t rule;           /* 0 = entropy bound, 1 = confidence threshold */
   float bound;            /* entropy bound (rule 0) or confidence threshold (rule 1), finite */
   uint32_t step;          /* denoising step: third Philox counter word */
+  int32_t noise;          /* 0 = one Gumbel per group of four entries (default), 1 = one per token */
   uint64_t seed;          /* Philox key */
 } moe_w4a16_sampler;
 

@@ -245,6 +245,7 @@ SAMPLER_VALID = dict(positions=8, vocab=4096, inv_temperature=1.0, rule=0, bound
     dict(positions=0), dict(positions=1025), dict(vocab=0), dict(vocab=4098), dict(vocab=(1 << 30) + 4),
     dict(inv_temperature=0.0), dict(inv_temperature=-1.0), dict(inv_temperature=float("inf")),
     dict(inv_temperature=float("nan")), dict(rule=2), dict(bound=float("nan")), dict(bound=float("inf")),
+    dict(noise=2), dict(noise=-1),
 ])
 def test_sampler_invalid_configs_rejected(bad):
     d = dict(SAMPLER_VALID)
@@ -258,12 +259,13 @@ def test_sampler_invalid_configs_rejected(bad):
 def test_sampler_host_validation():
     cfg = B.make_sampler(**SAMPLER_VALID)
     need = B.moe_w4a16_sampler_workspace_bytes(cfg)
-    def splits(P, V):  # about ceil(912 / P) splits, each a multiple of 2,048 elements
+    def splits(P, V):  # about ceil(912 / P) splits, each a multiple of 4,096 elements
         want = -(-912 // P)
-        chunk = -(-(-(-V // want)) // 2048) * 2048
+        chunk = -(-(-(-V // want)) // 4096) * 4096
         return -(-V // chunk)
-    assert need == 8 * splits(8, 4096) * 32 == 8 * 2 * 32  # one 32-byte partial per position and split
-    for P, V, S in ((8, 262144, 64), (256, 262144, 4), (64, 262144, 15), (1024, 262144, 1), (1, 4, 1)):
+    assert need == 8 * splits(8, 4096) * 32 == 8 * 1 * 32  # one 32-byte partial per position and split
+    for P, V, S in ((8, 262144, 64), (256, 262144, 4), (64, 262144, 13), (1024, 262144, 1), (1, 4, 1),
+                    (1, 1000000, 245), (600, 12300, 2)):
         assert splits(P, V) == S
         assert B.moe_w4a16_sampler_workspace_bytes(B.make_sampler(**dict(SAMPLER_VALID, positions=P, vocab=V))) == \
             P * S * 32
@@ -361,7 +363,7 @@ def test_smoke_sampler_check_with_a_host_stand_in():
 
     def fake_sample(cfg, logits, revealed, token, entropy, pmax, accept, workspace, stream=None):
         lg = logits.cpu().numpy()
-        t, e, pm = oracle.sample(lg, cfg.inv_temperature, cfg.seed, cfg.step, noise=1)
+        t, e, pm = oracle.sample(lg, cfg.inv_temperature, cfg.seed, cfg.step, noise=cfg.noise)
         token.copy_(torch.from_numpy(t))
         entropy.copy_(torch.from_numpy(e.astype(np.float32)))
         pmax.copy_(torch.from_numpy(pm.astype(np.float32)))

@@ -1,8 +1,10 @@
 """The per-step sampler through the C ABI against the CPU oracle (sampler_oracle.c).
 
-Bars:
+Both noise forms (0: one Gumbel per group of four entries, 1: one per token) are
+checked on every shape.  Bars:
   token     equal element for element (the Gumbel keys are defined in fp32 operation
-            by operation, so the argmax is the same integer on both sides);
+            by operation, so the argmax and the pick inside a group are the same
+            integers on both sides);
   entropy   |gpu - oracle| <= 2e-5 + 2e-5 |oracle| (fp32 streaming sums against fp64);
   pmax      relative 2e-5;
   accept    equal to the oracle's rule applied to the GPU's own fp32 entropy / pmax
@@ -43,9 +45,9 @@ def _logits(P, V, sigma, seed):
     return lg
 
 
-def _gpu_sample(B, lg, revealed, inv_temp, rule, bound, seed, step, repeats=1):
+def _gpu_sample(B, lg, revealed, inv_temp, rule, bound, seed, step, noise, repeats=1):
     P, V = lg.shape
-    cfg = B.make_sampler(P, V, inv_temp, rule, bound, step, seed)
+    cfg = B.make_sampler(P, V, inv_temp, rule, bound, step, seed, noise)
     ws = torch.empty(B.moe_w4a16_sampler_workspace_bytes(cfg), dtype=torch.uint8, device="cuda")
     d_lg = torch.from_numpy(lg).cuda()
     d_rev = torch.from_numpy(revealed).cuda()
@@ -61,9 +63,9 @@ def _gpu_sample(B, lg, revealed, inv_temp, rule, bound, seed, step, repeats=1):
     return [tuple(t.cpu().numpy() for t in o) for o in outs]
 
 
-def _check(lg, revealed, inv_temp, rule, bound, seed, step, got):
+def _check(lg, revealed, inv_temp, rule, bound, seed, step, noise, got):
     tok, ent, pm, acc = got
-    o_tok, o_ent, o_pm = oracle.sample(lg, inv_temp, seed, step, nthreads=NCPU, noise=1)
+    o_tok, o_ent, o_pm = oracle.sample(lg, inv_temp, seed, step, nthreads=NCPU, noise=noise)
     assert np.array_equal(tok, o_tok), np.nonzero(tok != o_tok)[0][:10]
     assert np.all(np.abs(ent.astype(np.float64) - o_ent) <= 2e-5 + 2e-5 * np.abs(o_ent)), \
         float(np.abs(ent - o_ent).max())
@@ -73,65 +75,103 @@ def _check(lg, revealed, inv_temp, rule, bound, seed, step, got):
     assert np.array_equal(acc, want)
 
 
+NOISE = pytest.mark.parametrize("noise", [0, 1], ids=["group", "token"])
+
+
+@NOISE
 @pytest.mark.parametrize("P,V,sigma,inv_temp,rule,bound", [
     (8, 4096, 1.0, 1.0, 0, 5.0),
-    (3, 4100, 3.0, 0.7, 1, 0.5),          # splits of 2,048: two full ones and a split of one float4
-    (5, 70000, 1.0, 1.0, 0, 30.0),        # ragged last split
-    (1, 4, 2.0, 1.3, 0, 0.0),             # smallest vocabulary: one split of one float4
-    (17, 65544, 3.0, 1.0, 1, 0.9),        # 32 full splits of 2,048 and one of 8 elements
+    (3, 4100, 3.0, 0.7, 1, 0.5),          # splits of 4,096: one full one and a split of one float4
+    (5, 70000, 1.0, 1.0, 0, 30.0),        # 17 splits of one block each (an odd block count), a ragged last split
+    (1, 4, 2.0, 1.3, 0, 0.0),             # smallest vocabulary: one split of one float4 (one group)
+    (17, 65544, 3.0, 1.0, 1, 0.9),        # 16 full splits of 4,096 and one of 8 elements
     (64, 32768, 1.0, 2.0, 0, 1.0),
     (6, 32772, 1.0, 1.0, 0, 2.0),
-    (9, 2060, 3.0, 1.0, 0, 3.0),          # a split of one full iteration (512 float4s) and one of 12 elements
-    (1, 1000000, 1.0, 1.0, 0, 2.0),       # one position cut into 489 splits: many partials to merge
+    (9, 2060, 3.0, 1.0, 0, 3.0),          # one split of 515 float4s: a full per-token iteration and 3 more; a partial block
+    (1, 1000000, 1.0, 1.0, 0, 2.0),       # one position cut into 245 splits: many partials to merge
     (3, 999996, 3.0, 1.0, 1, 0.5),        # 245 splits of 4,096 per position, the last one ragged
+    (600, 12300, 3.0, 1.0, 0, 20.0),      # splits of 8,192 (two blocks) and 4,108 (one block and 3 float4s)
+    (1000, 13000, 1.0, 0.9, 1, 0.3),      # one split: three full blocks and a partial one
 ], ids=lambda v: str(v))
-def test_sampler_matches_oracle(B, P, V, sigma, inv_temp, rule, bound):
+def test_sampler_matches_oracle(B, P, V, sigma, inv_temp, rule, bound, noise):
     lg = _logits(P, V, sigma, seed=P * 1000 + V)
     revealed = (np.arange(P) % 3 == 1).astype(np.uint8)
-    (got,) = _gpu_sample(B, lg, revealed, inv_temp, rule, bound, seed=0x1234_5678_9abc_def0 + P, step=V % 97)
-    _check(lg, revealed, inv_temp, rule, bound, 0x1234_5678_9abc_def0 + P, V % 97, got)
+    (got,) = _gpu_sample(B, lg, revealed, inv_temp, rule, bound, seed=0x1234_5678_9abc_def0 + P, step=V % 97,
+                         noise=noise)
+    _check(lg, revealed, inv_temp, rule, bound, 0x1234_5678_9abc_def0 + P, V % 97, noise, got)
 
 
-def test_sampler_ties_and_dominant_logits(B):
+@NOISE
+def test_sampler_ties_and_dominant_logits(B, noise):
     """Equal logits (the noise alone decides) and one overwhelming logit per position."""
     P, V = 6, 8192
     lg = np.zeros((P, V), np.float32)
     lg[3:, 100] = 60.0
     revealed = np.zeros(P, np.uint8)
-    (got,) = _gpu_sample(B, lg, revealed, 1.0, 0, 2.0, seed=9, step=3)
-    _check(lg, revealed, 1.0, 0, 2.0, 9, 3, got)
+    (got,) = _gpu_sample(B, lg, revealed, 1.0, 0, 2.0, seed=9, step=3, noise=noise)
+    _check(lg, revealed, 1.0, 0, 2.0, 9, 3, noise, got)
     assert np.all(got[0][3:] == 100)
 
 
+@NOISE
 @pytest.mark.parametrize("rule,bound", [(0, 40.0), (1, 0.5)])
-def test_sampler_full_canvas_step(B, rule, bound):
+def test_sampler_full_canvas_step(B, rule, bound, noise):
     """256 positions x 262,144 vocabulary (268 MB of fp32 logits), every position checked;
     three repeated calls bit-identical."""
     P, V = 256, 262144
     lg = _logits(P, V, 3.0, seed=rule)
     revealed = np.zeros(P, np.uint8)
     revealed[::4] = 1
-    outs = _gpu_sample(B, lg, revealed, 1.0, rule, bound, seed=77, step=5, repeats=3)
+    outs = _gpu_sample(B, lg, revealed, 1.0, rule, bound, seed=77, step=5, noise=noise, repeats=3)
     for o in outs[1:]:
         for a, b in zip(o, outs[0]):
             assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
-    _check(lg, revealed, 1.0, rule, bound, 77, 5, outs[0])
+    _check(lg, revealed, 1.0, rule, bound, 77, 5, noise, outs[0])
     assert outs[0][3].sum() >= 1
 
 
+@NOISE
 @pytest.mark.parametrize("rule,bound", [(0, 60.0), (1, 0.4)])
-def test_sampler_max_positions(B, rule, bound):
+def test_sampler_max_positions(B, rule, bound, noise):
     """P = 1024, the most positions one call takes (the final CTA holds one position
     per thread), over 16,384 tokens; every position checked."""
     P, V = 1024, 16384
     lg = _logits(P, V, 3.0, seed=1024 + rule)
     revealed = (np.arange(P) % 7 == 2).astype(np.uint8)
-    (got,) = _gpu_sample(B, lg, revealed, 1.0, rule, bound, seed=4242, step=11)
-    _check(lg, revealed, 1.0, rule, bound, 4242, 11, got)
+    (got,) = _gpu_sample(B, lg, revealed, 1.0, rule, bound, seed=4242, step=11, noise=noise)
+    _check(lg, revealed, 1.0, rule, bound, 4242, 11, noise, got)
 
 
-def test_sampler_all_revealed_accepts_nothing(B):
+@NOISE
+def test_sampler_all_revealed_accepts_nothing(B, noise):
     P, V = 4, 4096
     lg = _logits(P, V, 1.0, 5)
-    (got,) = _gpu_sample(B, lg, np.ones(P, np.uint8), 1.0, 0, 10.0, seed=1, step=0)
+    (got,) = _gpu_sample(B, lg, np.ones(P, np.uint8), 1.0, 0, 10.0, seed=1, step=0, noise=noise)
     assert got[3].sum() == 0
+
+
+def test_sampler_forms_sample_the_same_distribution(B):
+    """Both forms draw from softmax: over 8,192 positions with the same 64 logits (each
+    position its own counters), the token frequencies of each form pass a chi-square
+    test at p = 1e-4 against softmax, over the tokens with an expected count >= 5."""
+    scipy_stats = pytest.importorskip("scipy.stats")
+    rng = np.random.default_rng(21)
+    base = (rng.standard_normal(64) * 1.2).astype(np.float32)
+    P = 1024
+    p = np.exp(base.astype(np.float64))
+    p /= p.sum()
+    for noise in (0, 1):
+        counts = np.zeros(64)
+        for step in range(8):
+            (got,) = _gpu_sample(B, np.tile(base, (P, 1)), np.zeros(P, np.uint8), 1.0, 1, 0.99, seed=5, step=step,
+                                 noise=noise)
+            counts += np.bincount(got[0], minlength=64)
+        n = counts.sum()
+        keep = n * p >= 5
+        chi2 = float(((counts[keep] - n * p[keep]) ** 2 / (n * p[keep])).sum())
+        rest_o, rest_e = counts[~keep].sum(), n * p[~keep].sum()
+        dof = int(keep.sum()) - 1
+        if rest_e > 0:
+            chi2 += (rest_o - rest_e) ** 2 / rest_e
+            dof += 1
+        assert chi2 < scipy_stats.chi2.ppf(1 - 1e-4, dof), (noise, chi2, dof)

@@ -46,7 +46,7 @@ class Shape(ctypes.Structure):
 class Sampler(ctypes.Structure):
     _fields_ = [("positions", ctypes.c_int32), ("vocab", ctypes.c_int32), ("inv_temperature", ctypes.c_float),
                 ("rule", ctypes.c_int32), ("bound", ctypes.c_float), ("step", ctypes.c_uint32),
-                ("seed", ctypes.c_uint64)]
+                ("noise", ctypes.c_int32), ("seed", ctypes.c_uint64)]
 
 
 class Weights(ctypes.Structure):
@@ -265,8 +265,8 @@ def moe_w4a16_combine(shape: Shape, routing: RoutingBuffers, norm_gamma, norm_ep
            "moe_w4a16_combine")
 
 
-def make_sampler(positions, vocab, inv_temperature=1.0, rule=0, bound=0.0, step=0, seed=0) -> Sampler:
-    return Sampler(positions, vocab, inv_temperature, rule, bound, step, seed)
+def make_sampler(positions, vocab, inv_temperature=1.0, rule=0, bound=0.0, step=0, seed=0, noise=0) -> Sampler:
+    return Sampler(positions, vocab, inv_temperature, rule, bound, step, noise, seed)
 
 
 def moe_w4a16_sampler_workspace_bytes(cfg: Sampler) -> int:

@@ -113,7 +113,8 @@ namespace {
 bool sampler_ok(const moe_w4a16_sampler* c) {
   return c->positions >= 1 && c->positions <= moe::kSamplerMaxPositions && c->vocab >= 4 && c->vocab % 4 == 0 &&
          c->vocab <= (1 << 30) && c->inv_temperature > 0.f && c->inv_temperature <= 3.4e38f &&
-         (c->rule == 0 || c->rule == 1) && c->bound >= -3.4e38f && c->bound <= 3.4e38f;
+         (c->rule == 0 || c->rule == 1) && c->bound >= -3.4e38f && c->bound <= 3.4e38f &&
+         (c->noise == 0 || c->noise == 1);
 }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 }  // namespace
@@ -136,8 +137,8 @@ moe_w4a16_status moe_w4a16_sample(const moe_w4a16_sampler* cfg, const float* log
   const DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != MOE_W4A16_OK) return st;
   return cuda_status(moe::launch_sample(cfg->positions, cfg->vocab, cfg->inv_temperature, cfg->seed, cfg->step,
-                                        cfg->rule, cfg->bound, logits, revealed, token, entropy, pmax, accept,
-                                        workspace, static_cast<cudaStream_t>(stream)));
+                                        cfg->rule, cfg->bound, cfg->noise, logits, revealed, token, entropy, pmax,
+                                        accept, workspace, static_cast<cudaStream_t>(stream)));
 }
 
 moe_w4a16_status moe_w4a16_route(const moe_w4a16_shape* shape, const float* logits, const moe_w4a16_routing* out,

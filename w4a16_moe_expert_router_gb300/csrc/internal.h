@@ -155,12 +155,13 @@ cudaError_t launch_block_front(const Dims& s, const uint16_t* x, const float* ga
 constexpr int kSamplerMaxPositions = 1024;  // one thread per position in the final CTA
 // Vocabulary elements per CTA of the pass: the vocabulary is cut into about
 // ceil(912 / positions) splits (912 CTAs: two waves of three 256-thread CTAs on
-// each of 152 SMs), each a multiple of 2,048 elements (one iteration of a CTA).
+// each of 152 SMs), each a multiple of 4,096 elements (a block of the per-group pass,
+// whose 1,024 groups share 256 Philox counters; two iterations of the per-token pass).
 // Fewer, longer CTAs amortise each CTA's start and final reduction.
 inline int64_t sampler_chunk(int positions, int64_t vocab) {
   const int64_t want = (912 + positions - 1) / positions;
   const int64_t per = (vocab + want - 1) / want;
-  return (per + 2047) / 2048 * 2048;
+  return (per + 4095) / 4096 * 4096;
 }
 inline int sampler_splits(int positions, int64_t vocab) {
   return static_cast<int>((vocab + sampler_chunk(positions, vocab) - 1) / sampler_chunk(positions, vocab));
@@ -169,7 +170,7 @@ inline size_t sampler_ws_bytes(int positions, int64_t vocab) {
   return size_t(positions) * size_t(sampler_splits(positions, vocab)) * 32;
 }
 cudaError_t launch_sample(int P, int64_t V, float inv_temp, uint64_t seed, uint32_t step, int rule, float bound,
-                          const float* logits, const uint8_t* revealed, int32_t* token, float* entropy, float* pmax,
+                          int noise, const float* logits, const uint8_t* revealed, int32_t* token, float* entropy, float* pmax,
                           uint8_t* accept, void* workspace, cudaStream_t st);
 
 // Self-test of the expert launch's bounded waits: waits that cannot complete (an

@@ -10,35 +10,43 @@
 // entropy-bound acceptance (positions by ascending entropy, the mlx-vlm rule
 // (cumsum - cummax) <= bound, at least one) or confidence-threshold acceptance.
 //
-// Gumbel-max: token = argmax_v (t_v + G_v), t_v = logit_v * inv_temp,
-// G_v = -ln(-ln U_v), U_v = ((x & 0x7fffff) + 1/2) 2^-23 from word v % 4 of
-// Philox4x32-10 (Salmon et al., SC'11) at counter (v / 4, position, step, 0) under
-// key (seed low, seed high); ties to the lower index.  The key decides an
-// integer, so it is computed with one IEEE fp32 rounding per operation (ln_f32
-// below, then fma(logit, inv_temp, G)): any implementation that takes these
-// steps gets the same token.
+// Gumbel-max, two forms (both sample softmax(t), t_v = logit_v * inv_temp):
+//   noise 1, one Gumbel per token: token = argmax_v (t_v + G_v), G_v = -ln(-ln U_v),
+//     U_v = ((x & 0x7fffff) + 1/2) 2^-23 from word v % 4 of Philox4x32-10 (Salmon et al.,
+//     SC'11) at counter (v / 4, position, step, 0) under key (seed low, seed high); ties to
+//     the lower index; key = fma(logit, inv_temp, G).
+//   noise 0, one Gumbel per group of four entries (the default): the largest of four
+//     independent Gumbel keys is Gumbel around the group's log-sum-exp, and where it
+//     falls is softmax within the group (max-stability of the Gumbel law), so group
+//     g = entries 4g .. 4g+3 gets the key LSE_g + G_g, the winning group is the argmax
+//     (ties to the lower group) and the token inside it is drawn by inverse CDF from a
+//     second uniform.  U_g is word r / 256 of counter (256 (g / 1024) + r % 256,
+//     position, step, 0), r = g % 1024, so that one Philox call serves the four groups a
+//     thread holds (float4s 256 apart); U'_g the same word with fourth counter word 1.
+// Every key decides an integer, so it is computed with one IEEE fp32 rounding per
+// operation (ln_f32 and exp_f32 below): any implementation that takes these steps gets
+// the same token.
 //
 // Pass kernel (grid: vocabulary splits x positions, 256 threads): each thread
 // streams float4s of its position's logits and keeps, in base 2, the running
 // maximum m2 of t2 = t log2(e), Z = sum 2^(t2 - m2) and S1 = sum 2^(t2 - m2)(t2 - m2).
-// Computing the exact key of every element would cost two logarithms each and
-// make the pass arithmetic-bound, so a cheap necessary condition screens them:
-// with K the best exact key the CTA has found so far, element v can reach K only
-// if w_v = 1 - U_v <= e^(t_v - K) (because -ln U >= 1 - U, and G = -ln(-ln U));
-// the test is made with a margin that covers every rounding involved (fast
-// exponentials included), and only the elements that pass it (a few per warp
-// over the pass) get their exact key.  The test reuses 2^(t2 - m2) of the
-// softmax sum, so an element costs one Philox quarter, one exp2 and about eight
-// other instructions.  A thread takes two float4s per iteration (eight elements,
-// one check of the screening factor) and loads them two iterations ahead with
-// streaming 16-byte loads into registers, so four loads per thread are in flight
-// and nothing waits on shared memory or a barrier.  Each CTA
-// writes its partial (m2, Z, S1, best key, index).
+// Exact keys cost logarithms (and, per group, four exponentials), so a cheap
+// necessary condition screens them: with K the best exact key the CTA has found so
+// far, a token (group) can reach K only if w = 1 - U <= e^(t - K) (the group's sum of
+// e^(t_i - K)), because -ln U >= 1 - U and G = -ln(-ln U); the test is made with a
+// margin that covers every rounding involved (fast exponentials included) and reuses
+// 2^(t2 - m2) of the softmax sum; only the few that pass get their exact key.  Per
+// token, an element costs one Philox quarter, one exp2 and about eight other
+// instructions; per group, a Philox call serves sixteen elements and the screen runs
+// once per four, so the pass streams at memory speed.  Loads are streaming 16-byte
+// loads into registers, issued one to two iterations ahead; nothing waits on shared
+// memory or a barrier.  Each CTA writes its partial (m2, Z, S1, best key, token or group).
 //
 // Final kernel (one CTA, one thread per position): merges each position's
-// partials in split order, writes token, entropy H = ln Z - (S1 / Z) ln 2 and
-// top-1 probability 1 / Z, then applies the acceptance rule to those fp32
-// values (entropy rule: rank by (H, position), then one thread runs the fp32
+// partials in split order, writes entropy H = ln Z - (S1 / Z) ln 2, top-1
+// probability 1 / Z and the token (per group: the inverse-CDF pick inside the winning
+// group, from its four logits), then applies the acceptance rule to those fp32
+// values (entropy rule: rank by (H, position), then one warp runs the fp32
 // cumulative sum and maximum in sorted order).
 #include <cuda_runtime.h>
 
@@ -170,6 +178,57 @@ __device__ __forceinline__ void merge_sums(float& m2, float& z, float& s1, float
   m2 = m;
 }
 
+// e^x for x <= 0 as a fixed sequence of IEEE fp32 operations: n = rint(x log2 e),
+// r = (x - n ln2_hi) - n ln2_lo (ln2_hi = ln 2 to 16 bits, so n ln2_hi is exact),
+// e^r by its Taylor series to r^7 (Horner with fused multiply-adds, coefficients
+// the fp32 quotients 1/5040 ... 1/2), times 2^n built from exponent bits.  Below
+// -87 the result is defined as 0 (2^n would leave the normal range).
+__device__ __forceinline__ float exp_f32(float x) {
+  if (!(x >= -87.f)) return 0.f;
+  const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));
+  float r = __fmaf_rn(-n, 0x1.62e4p-1f, x);
+  r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);
+  float p = 0x1.a01a02p-13f;             // 1/5040
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/720
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);   // 1/120
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);   // 1/24
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);   // 1/6
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  return __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(static_cast<int>(n) + 127) << 23));
+}
+
+// A group of four logits (one float4, vocabulary entries 4g .. 4g+3) in fp32 operations:
+// t_i = fl(l_i inv_temp), m = max t_i, e_i = e^(t_i - m) (exp_f32), S = ((e_0 + e_1) + e_2) + e_3.
+struct GroupExp {
+  float m, e[4], s;
+};
+__device__ __forceinline__ GroupExp group_exp(float4 l, float inv_temp) {
+  GroupExp g;
+  const float t[4] = {__fmul_rn(l.x, inv_temp), __fmul_rn(l.y, inv_temp), __fmul_rn(l.z, inv_temp),
+                      __fmul_rn(l.w, inv_temp)};
+  g.m = fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) g.e[i] = exp_f32(__fsub_rn(t[i], g.m));
+  g.s = __fadd_rn(__fadd_rn(__fadd_rn(g.e[0], g.e[1]), g.e[2]), g.e[3]);
+  return g;
+}
+
+// Exact key of a group: fl(fl(m + ln S) + G), G = -ln(-ln U) of its Philox word.
+__device__ __forceinline__ float group_key(float4 l, float inv_temp, uint32_t word) {
+  const GroupExp g = group_exp(l, inv_temp);
+  const float u = __fmul_rn(__fadd_rn(static_cast<float>(word & 0x007fffffu), 0.5f), 0x1p-23f);
+  const float gum = -ln_f32(-ln_f32(u));
+  return __fadd_rn(__fadd_rn(g.m, ln_f32(g.s)), gum);
+}
+
+// Philox counter word 0 of group g (float4 index in the position's row): the groups of
+// each 4,096-entry block share 256 counters, group r of the block taking word r / 256
+// of counter 256 * block + r % 256.
+__device__ __forceinline__ uint32_t group_counter(uint32_t g) { return ((g >> 10) << 8) | (g & 255u); }
+__device__ __forceinline__ int group_word(uint32_t g) { return static_cast<int>((g >> 8) & 3u); }
+
 // Running state of one pass thread.
 struct PassState {
   float m2, z, s1;     // base-2 online softmax sums
@@ -259,28 +318,102 @@ __device__ __forceinline__ void pass_iter(PassState& S, const float4 (&x)[2], in
   }
 }
 
-__global__ void __launch_bounds__(kPassThreads, 3)
-    sample_pass_kernel(const float* __restrict__ logits, int64_t V, int chunk, float inv_temp, uint32_t k0,
-                       uint32_t k1, uint32_t step, Partial* __restrict__ part) {
-  __shared__ uint32_t cta_best;  // encoded best exact key of the CTA so far
-  __shared__ float red_f[kPassThreads / 32][4];
-  __shared__ int32_t red_v[kPassThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int s = blockIdx.x, p = blockIdx.y;
-  if (tid == 0) cta_best = key_enc(-INFINITY);
-  grid_dependents_launch();  // the final launch may set up meanwhile; it waits for this one
-  grid_dependency_wait();    // the logits of the launch before
-  __syncthreads();
-  const int64_t v0 = static_cast<int64_t>(s) * chunk;
-  const int n4 = static_cast<int>((min(V, v0 + chunk) - v0) / 4);
-  const float4* src = reinterpret_cast<const float4*>(logits + static_cast<int64_t>(p) * V + v0);
+// Sixteen logits of one thread: float4s j + 256 q (q = 0..3) of a 4,096-entry block, the
+// four groups of Philox counter cnt (group q takes word q).  With kGuard, float4s at or
+// past n4 take no part (the range's last, partial block).
+template <bool kGuard>
+__device__ __forceinline__ void pass_block(PassState& S, const float4 (&x)[4], int j, int n4, uint32_t gbase,
+                                           uint32_t cnt, uint32_t p, uint32_t step, const PhiloxKeys& pk, float c2e,
+                                           float inv_temp, volatile uint32_t* vbest, uint32_t* cta_best) {
+  uint32_t w[4];
+  philox4x32_10(cnt, p, step, 0u, pk, w);
+  bool act[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) act[q] = !kGuard || j + q * kPassThreads < n4;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (act[q]) mx = fmaxf(mx, fmaxf(fmaxf(x[q].x, x[q].y), fmaxf(x[q].z, x[q].w)));
+  mx *= c2e;
+  if (mx > S.m2) {
+    if (S.z != 0.f) {
+      const float dm = S.m2 - mx;
+      const float r = fast_exp2(dm);
+      S.s1 = r * fmaf(dm, S.z, S.s1);
+      S.z *= r;
+    }
+    S.m2 = mx;
+  }
+  // screen: group g can reach the best key K only if w_g = 1 - U_g <= sum_i e^(t_i - K)
+  // (its key is ln sum_i e^(t_i) - ln(-ln U_g) and -ln U >= 1 - U), tested as
+  // w_g <= zg c2 with zg = sum_i 2^(t2_i - m2) and c2 = 2^(m2 - K2 + slack) 1.01; the slack
+  // covers the roundings of t2, K2, the group's exact sum and logarithm, and the fast exp2
+  const float K = key_dec(*vbest);
+  if (K != S.c_K || S.m2 != S.c_m2) {
+    S.c_K = K;
+    S.c_m2 = S.m2;
+    S.c2 = 3e38f;
+    if (K != -INFINITY) {
+      const float K2 = K * 1.44269504088896341f;
+      const float slack = 0x1p-8f + (fabsf(S.m2) + fabsf(K2)) * 0x1p-14f;
+      S.c2 = fminf(fast_exp2(S.m2 - K2 + slack) * 1.01f, 3e38f);
+    }
+  }
+  // f_g + zg c2 >= 2 - 2^-23 with f_g = 1 + (x & 0x7fffff) 2^-23 is implied by w_g <= zg c2
+  float qmax = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (!act[q]) continue;
+    const float l[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+    float e[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float d = fmaf(l[i], c2e, -S.m2);
+      e[i] = fast_exp2(d);
+      S.s1 = fmaf(e[i], d, S.s1);
+    }
+    const float zg = (e[0] + e[1]) + (e[2] + e[3]);
+    S.z += zg;
+    const float f = __uint_as_float(0x3f800000u | (w[q] & 0x007fffffu));
+    qmax = fmaxf(qmax, fmaf(zg, S.c2, f));
+  }
+  const bool any = qmax >= 0x1.fffffep+0f;
+  if (__any_sync(0xffffffffu, any)) {
+    if (any) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (!act[q]) continue;
+        const float l[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+        float zg = 0.f;
+        {
+          float e[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) e[i] = fast_exp2(fmaf(l[i], c2e, -S.m2));
+          zg = (e[0] + e[1]) + (e[2] + e[3]);
+        }
+        const float f = __uint_as_float(0x3f800000u | (w[q] & 0x007fffffu));
+        if (!(fmaf(zg, S.c2, f) >= 0x1.fffffep+0f)) continue;
+        const float k = group_key(x[q], inv_temp, w[q]);
+        const int32_t g = static_cast<int32_t>(gbase + static_cast<uint32_t>(j + q * kPassThreads));
+        if (better(k, g, S.bk, S.bv)) {
+          S.bk = k;
+          S.bv = g;
+        }
+      }
+      atomicMax(cta_best, key_enc(S.bk));
+    }
+  }
+}
+
+// The per-token pass over float4s [0, n4) of the CTA's range: iteration it covers
+// float4s it * 512 + tid and + 256; the loads run two iterations ahead over three
+// register buffers, streaming (evict-first), from addresses clamped into the range
+// (a load past its end is never used).
+__device__ __forceinline__ void run_tokens(PassState& S, const float4* src, int n4, int64_t v0, uint32_t p,
+                                           uint32_t step, const PhiloxKeys& pk, float c2e, float inv_temp,
+                                           uint32_t* cta_best) {
+  const int tid = threadIdx.x;
   const uint32_t g0 = static_cast<uint32_t>(v0 / 4);
-  const float c2e = inv_temp * 1.44269504088896341f;  // screening only
-  const PhiloxKeys pk = philox_keys(k0, k1);
-  PassState S{-INFINITY, 0.f, 0.f, -INFINITY, 0x7fffffff, 3e38f, NAN, NAN};
-  // iteration it covers float4s j = it * 512 + tid and j + 256; the loads run two
-  // iterations ahead, streaming (evict-first), from addresses clamped into the range
-  // (a load past its end is never used)
   constexpr int kStep = 2 * kPassThreads;
   const int n_full = n4 / kStep, n_iter = (n4 + kStep - 1) / kStep;
   const int last4 = max(n4 - 1, 0);
@@ -299,13 +432,13 @@ __global__ void __launch_bounds__(kPassThreads, 3)
     if (ib >= 0) {
       const int j = tid + (ib / 4) * kPassThreads;
       uint32_t w[4];
-      philox4x32_10(g0 + static_cast<uint32_t>(j), static_cast<uint32_t>(p), step, 0u, pk, w);
-      const float lb = ib == 0 ? l[0] : ib == 1 ? l[1] : ib == 2 ? l[2] : ib == 3 ? l[3]
-                     : ib == 4 ? l[4] : ib == 5 ? l[5] : ib == 6 ? l[6] : l[7];
+      philox4x32_10(g0 + static_cast<uint32_t>(j), p, step, 0u, pk, w);
+      const float lmax = ib == 0 ? l[0] : ib == 1 ? l[1] : ib == 2 ? l[2] : ib == 3 ? l[3]
+                       : ib == 4 ? l[4] : ib == 5 ? l[5] : ib == 6 ? l[6] : l[7];
       const uint32_t wb = (ib & 3) == 0 ? w[0] : (ib & 3) == 1 ? w[1] : (ib & 3) == 2 ? w[2] : w[3];
-      S.bk = gumbel_key(lb, inv_temp, wb);
+      S.bk = gumbel_key(lmax, inv_temp, wb);
       S.bv = static_cast<int32_t>(v0 + 4 * static_cast<int64_t>(j) + (ib & 3));
-      atomicMax(&cta_best, key_enc(S.bk));
+      atomicMax(cta_best, key_enc(S.bk));
     }
     __syncthreads();
   }
@@ -317,33 +450,119 @@ __global__ void __launch_bounds__(kPassThreads, 3)
     const int j = it * kStep + tid;
     third[0] = load(j + 2 * kStep);
     third[1] = load(j + 2 * kStep + kPassThreads);
-    pass_iter<false>(S, cur, j, n4, v0, g0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp, &cta_best,
-                     &cta_best);
+    pass_iter<false>(S, cur, j, n4, v0, g0, p, step, pk, c2e, inv_temp, cta_best, cta_best);
     cur[0] = load(j + 3 * kStep);
     cur[1] = load(j + 3 * kStep + kPassThreads);
-    pass_iter<false>(S, nxt, j + kStep, n4, v0, g0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp, &cta_best,
-                     &cta_best);
+    pass_iter<false>(S, nxt, j + kStep, n4, v0, g0, p, step, pk, c2e, inv_temp, cta_best, cta_best);
     nxt[0] = load(j + 4 * kStep);
     nxt[1] = load(j + 4 * kStep + kPassThreads);
-    pass_iter<false>(S, third, j + 2 * kStep, n4, v0, g0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp,
-                     &cta_best, &cta_best);
+    pass_iter<false>(S, third, j + 2 * kStep, n4, v0, g0, p, step, pk, c2e, inv_temp, cta_best, cta_best);
   }
   for (; it < n_full; ++it) {  // the last full iterations, one at a time
     const int j = it * kStep + tid;
     const float4 pf0 = load(j + 2 * kStep), pf1 = load(j + 2 * kStep + kPassThreads);
-    pass_iter<false>(S, cur, j, n4, v0, g0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp, &cta_best,
-                     &cta_best);
+    pass_iter<false>(S, cur, j, n4, v0, g0, p, step, pk, c2e, inv_temp, cta_best, cta_best);
     cur[0] = nxt[0];
     cur[1] = nxt[1];
     nxt[0] = pf0;
     nxt[1] = pf1;
   }
   if (it < n_iter)  // the range's last, partial iteration
-    pass_iter<true>(S, cur, it * kStep + tid, n4, v0, g0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp,
-                    &cta_best, &cta_best);
+    pass_iter<true>(S, cur, it * kStep + tid, n4, v0, g0, p, step, pk, c2e, inv_temp, cta_best, cta_best);
+}
+
+// The per-group pass over float4s [0, n4) of the CTA's range (v0 a multiple of 4,096):
+// block b covers float4s b * 1024 + tid + 256 q (q = 0..3), the four groups of one
+// Philox counter; the loads run one block ahead over two register buffers.
+__device__ __forceinline__ void run_groups(PassState& S, const float4* src, int n4, int64_t v0, uint32_t p,
+                                           uint32_t step, const PhiloxKeys& pk, float c2e, float inv_temp,
+                                           uint32_t* cta_best) {
+  const int tid = threadIdx.x;
+  const uint32_t gbase = static_cast<uint32_t>(v0 / 4);
+  const uint32_t cnt0 = ((gbase >> 10) << 8) | static_cast<uint32_t>(tid);  // counter of the thread's first block
+  constexpr int kBlk = 4 * kPassThreads;
+  const int n_full = n4 / kBlk, n_blk = (n4 + kBlk - 1) / kBlk;
+  const int last4 = max(n4 - 1, 0);
+  auto load = [&](int j) { return __ldcs(src + min(j, last4)); };
+  float4 A[4], B[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) A[q] = load(tid + q * kPassThreads);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) B[q] = load(kBlk + tid + q * kPassThreads);
+  {
+    // a first threshold for the screen: the exact key of the thread's first group with
+    // the largest logit (any group's exact key is a valid threshold)
+    int qb = -1;
+    float lb = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float mq = fmaxf(fmaxf(A[q].x, A[q].y), fmaxf(A[q].z, A[q].w));
+      if (tid + q * kPassThreads < n4 && (qb < 0 || mq > lb)) {
+        qb = q;
+        lb = mq;
+      }
+    }
+    if (qb >= 0) {
+      uint32_t w[4];
+      philox4x32_10(cnt0, p, step, 0u, pk, w);
+      const float4 xb = qb == 0 ? A[0] : qb == 1 ? A[1] : qb == 2 ? A[2] : A[3];
+      const uint32_t wb = qb == 0 ? w[0] : qb == 1 ? w[1] : qb == 2 ? w[2] : w[3];
+      S.bk = group_key(xb, inv_temp, wb);
+      S.bv = static_cast<int32_t>(gbase + static_cast<uint32_t>(tid + qb * kPassThreads));
+      atomicMax(cta_best, key_enc(S.bk));
+    }
+    __syncthreads();
+  }
+  int b = 0;
+  for (; b + 2 <= n_full; b += 2) {  // uniform trip count; two blocks per trip over two buffers
+    const int j = b * kBlk + tid;
+    pass_block<false>(S, A, j, n4, gbase, cnt0 + (static_cast<uint32_t>(b) << 8), p, step, pk, c2e, inv_temp,
+                      cta_best, cta_best);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) A[q] = load(j + 2 * kBlk + q * kPassThreads);
+    pass_block<false>(S, B, j + kBlk, n4, gbase, cnt0 + (static_cast<uint32_t>(b + 1) << 8), p, step, pk, c2e,
+                      inv_temp, cta_best, cta_best);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) B[q] = load(j + 3 * kBlk + q * kPassThreads);
+  }
+  if (b < n_full) {  // an odd last full block
+    pass_block<false>(S, A, b * kBlk + tid, n4, gbase, cnt0 + (static_cast<uint32_t>(b) << 8), p, step, pk, c2e,
+                      inv_temp, cta_best, cta_best);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) A[q] = B[q];
+    ++b;
+  }
+  if (b < n_blk)  // the range's last, partial block
+    pass_block<true>(S, A, b * kBlk + tid, n4, gbase, cnt0 + (static_cast<uint32_t>(b) << 8), p, step, pk, c2e,
+                     inv_temp, cta_best, cta_best);
+}
+
+template <int kNoise>
+__global__ void __launch_bounds__(kPassThreads, 3)
+    sample_pass_kernel(const float* __restrict__ logits, int64_t V, int chunk, float inv_temp, uint32_t k0,
+                       uint32_t k1, uint32_t step, Partial* __restrict__ part) {
+  __shared__ uint32_t cta_best;  // encoded best exact key of the CTA so far
+  __shared__ float red_f[kPassThreads / 32][4];
+  __shared__ int32_t red_v[kPassThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s = blockIdx.x, p = blockIdx.y;
+  if (tid == 0) cta_best = key_enc(-INFINITY);
+  grid_dependents_launch();  // the final launch may set up meanwhile; it waits for this one
+  grid_dependency_wait();    // the logits of the launch before
+  __syncthreads();
+  const int64_t v0 = static_cast<int64_t>(s) * chunk;
+  const int n4 = static_cast<int>((min(V, v0 + chunk) - v0) / 4);
+  const float4* src = reinterpret_cast<const float4*>(logits + static_cast<int64_t>(p) * V + v0);
+  const float c2e = inv_temp * 1.44269504088896341f;  // screening only
+  const PhiloxKeys pk = philox_keys(k0, k1);
+  PassState S{-INFINITY, 0.f, 0.f, -INFINITY, 0x7fffffff, 3e38f, NAN, NAN};
+  if (kNoise == 0)
+    run_groups(S, src, n4, v0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp, &cta_best);
+  else
+    run_tokens(S, src, n4, v0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp, &cta_best);
   float m2 = S.m2, z = S.z, s1 = S.s1, bk = S.bk;
   int32_t bv = S.bv;
-  // reduce: sums and the best (key, index), lanes then warps in a fixed order
+  // reduce: sums and the best (key, token or group), lanes then warps in a fixed order
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const float om2 = __shfl_down_sync(0xffffffffu, m2, off);
@@ -395,7 +614,9 @@ __device__ __forceinline__ float asc_dec(uint32_t u) {
 }
 
 __global__ void __launch_bounds__(kFinalThreads)
-    sample_final_kernel(const Partial* __restrict__ part, int P, int S, int rule, float bound,
+    sample_final_kernel(const Partial* __restrict__ part, int P, int S, int rule, float bound, int noise,
+                        const float* __restrict__ logits, int64_t V, float inv_temp, uint32_t k0, uint32_t k1,
+                        uint32_t step,
                         const uint8_t* __restrict__ revealed, int32_t* __restrict__ token, float* __restrict__ entropy,
                         float* __restrict__ pmax, uint8_t* __restrict__ accept) {
   __shared__ unsigned long long keys[kFinalThreads];  // rule 0: (entropy, position), sorted ascending
@@ -433,7 +654,31 @@ __global__ void __launch_bounds__(kFinalThreads)
     h = logf(z) - (s1 / z) * 0.693147180559945309f;
     pm = 1.f / z;
     rev = revealed[p] != 0;
-    token[p] = bv;
+    // per group, the token inside the winning group: the first i whose running sum
+    // fl(..fl(e_0 + e_1).. + e_i) exceeds fl(U' S), U' from the group's word of its
+    // counter with fourth word 1; if none does, the last i with e_i > 0
+    if (noise == 0) {
+      const uint32_t g = static_cast<uint32_t>(bv);
+      const float4 l = __ldg(reinterpret_cast<const float4*>(logits + static_cast<int64_t>(p) * V) + g);
+      const GroupExp ge = group_exp(l, inv_temp);
+      uint32_t w[4];
+      philox4x32_10(group_counter(g), static_cast<uint32_t>(p), step, 1u, philox_keys(k0, k1), w);
+      const uint32_t x = w[group_word(g)];
+      const float u = __fmul_rn(__fadd_rn(static_cast<float>(x & 0x007fffffu), 0.5f), 0x1p-23f);
+      const float T = __fmul_rn(u, ge.s);
+      int pick = -1, last = 0;
+      float c = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        c = i == 0 ? ge.e[0] : __fadd_rn(c, ge.e[i]);
+        if (pick < 0 && c > T) pick = i;
+        if (ge.e[i] > 0.f) last = i;
+      }
+      token[p] = static_cast<int32_t>(4 * g) + (pick < 0 ? last : pick);
+    }
+    else {
+      token[p] = bv;
+    }
     entropy[p] = h;
     pmax[p] = pm;
   }
@@ -525,16 +770,19 @@ __global__ void __launch_bounds__(kFinalThreads)
 
 
 cudaError_t launch_sample(int P, int64_t V, float inv_temp, uint64_t seed, uint32_t step, int rule, float bound,
-                          const float* logits, const uint8_t* revealed, int32_t* token, float* entropy, float* pmax,
+                          int noise, const float* logits, const uint8_t* revealed, int32_t* token, float* entropy, float* pmax,
                           uint8_t* accept, void* workspace, cudaStream_t st) {
   const int S = sampler_splits(P, V);
   const int chunk = static_cast<int>(sampler_chunk(P, V));
   auto* part = static_cast<Partial*>(workspace);
-  cudaError_t e = launch_pdl(sample_pass_kernel, dim3(S, P), dim3(kPassThreads), 0, st, logits, V, chunk,
-                             inv_temp, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), step, part);
+  const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  cudaError_t e = noise == 0 ? launch_pdl(sample_pass_kernel<0>, dim3(S, P), dim3(kPassThreads), 0, st, logits, V,
+                                          chunk, inv_temp, k0, k1, step, part)
+                             : launch_pdl(sample_pass_kernel<1>, dim3(S, P), dim3(kPassThreads), 0, st, logits, V,
+                                          chunk, inv_temp, k0, k1, step, part);
   if (e != cudaSuccess) return e;
   return launch_pdl(sample_final_kernel, dim3(1), dim3(kFinalThreads), 0, st, static_cast<const Partial*>(part), P, S,
-                    rule, bound, revealed, token, entropy, pmax, accept);
+                    rule, bound, noise, logits, V, inv_temp, k0, k1, step, revealed, token, entropy, pmax, accept);
 }
 
 }  // namespace moe
