@@ -46,8 +46,8 @@
 // partials in split order, writes entropy H = ln Z - (S1 / Z) ln 2, top-1
 // probability 1 / Z and the token (per group: the inverse-CDF pick inside the winning
 // group, from its four logits), then applies the acceptance rule to those fp32
-// values (entropy rule: rank by (H, position), then one warp runs the fp32
-// cumulative sum and maximum in sorted order).
+// values (entropy rule: a bitonic sort by (H, position), then one thread runs the
+// fp32 cumulative sum in sorted order and every thread decides its own entry).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -223,6 +223,24 @@ __device__ __forceinline__ float group_key(float4 l, float inv_temp, uint32_t wo
   return __fadd_rn(__fadd_rn(g.m, ln_f32(g.s)), gum);
 }
 
+// The token inside a group (0 .. 3) by inverse CDF: T = fl(U' S) with U' from the
+// word, the first i whose running sum fl(..fl(e_0 + e_1).. + e_i) exceeds T; if none
+// does (T rounded up to S), the last i with e_i > 0.
+__device__ __forceinline__ int group_pick(float4 l, float inv_temp, uint32_t word) {
+  const GroupExp ge = group_exp(l, inv_temp);
+  const float u = __fmul_rn(__fadd_rn(static_cast<float>(word & 0x007fffffu), 0.5f), 0x1p-23f);
+  const float T = __fmul_rn(u, ge.s);
+  int pick = -1, last = 0;
+  float c = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    c = i == 0 ? ge.e[0] : __fadd_rn(c, ge.e[i]);
+    if (pick < 0 && c > T) pick = i;
+    if (ge.e[i] > 0.f) last = i;
+  }
+  return pick < 0 ? last : pick;
+}
+
 // Philox counter word 0 of group g (float4 index in the position's row): the groups of
 // each 4,096-entry block share 256 counters, group r of the block taking word r / 256
 // of counter 256 * block + r % 256.
@@ -232,9 +250,10 @@ __device__ __forceinline__ int group_word(uint32_t g) { return static_cast<int>(
 // Running state of one pass thread.
 struct PassState {
   float m2, z, s1;     // base-2 online softmax sums
-  float bk;            // best exact key so far, and its token
+  float bk;            // best exact key so far, and its token (per group: its group)
   int32_t bv;
   float c2, c_K, c_m2;  // screening factor and the (K, m2) it was made for
+  float4 bl;            // per group: the best group's four logits
 };
 
 // Eight elements of one thread: float4s j and j + 256 of the CTA's range (ids
@@ -398,6 +417,7 @@ __device__ __forceinline__ void pass_block(PassState& S, const float4 (&x)[4], i
         if (better(k, g, S.bk, S.bv)) {
           S.bk = k;
           S.bv = g;
+          S.bl = x[q];
         }
       }
       atomicMax(cta_best, key_enc(S.bk));
@@ -509,6 +529,7 @@ __device__ __forceinline__ void run_groups(PassState& S, const float4* src, int 
       const uint32_t wb = qb == 0 ? w[0] : qb == 1 ? w[1] : qb == 2 ? w[2] : w[3];
       S.bk = group_key(xb, inv_temp, wb);
       S.bv = static_cast<int32_t>(gbase + static_cast<uint32_t>(tid + qb * kPassThreads));
+      S.bl = xb;
       atomicMax(cta_best, key_enc(S.bk));
     }
     __syncthreads();
@@ -544,6 +565,7 @@ __global__ void __launch_bounds__(kPassThreads, 3)
   __shared__ uint32_t cta_best;  // encoded best exact key of the CTA so far
   __shared__ float red_f[kPassThreads / 32][4];
   __shared__ int32_t red_v[kPassThreads / 32];
+  __shared__ float4 red_l[kPassThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x, p = blockIdx.y;
   if (tid == 0) cta_best = key_enc(-INFINITY);
@@ -555,13 +577,14 @@ __global__ void __launch_bounds__(kPassThreads, 3)
   const float4* src = reinterpret_cast<const float4*>(logits + static_cast<int64_t>(p) * V + v0);
   const float c2e = inv_temp * 1.44269504088896341f;  // screening only
   const PhiloxKeys pk = philox_keys(k0, k1);
-  PassState S{-INFINITY, 0.f, 0.f, -INFINITY, 0x7fffffff, 3e38f, NAN, NAN};
+  PassState S{-INFINITY, 0.f, 0.f, -INFINITY, 0x7fffffff, 3e38f, NAN, NAN, make_float4(0.f, 0.f, 0.f, 0.f)};
   if (kNoise == 0)
     run_groups(S, src, n4, v0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp, &cta_best);
   else
     run_tokens(S, src, n4, v0, static_cast<uint32_t>(p), step, pk, c2e, inv_temp, &cta_best);
   float m2 = S.m2, z = S.z, s1 = S.s1, bk = S.bk;
   int32_t bv = S.bv;
+  float4 bl = S.bl;
   // reduce: sums and the best (key, token or group), lanes then warps in a fixed order
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -570,10 +593,18 @@ __global__ void __launch_bounds__(kPassThreads, 3)
     const float os1 = __shfl_down_sync(0xffffffffu, s1, off);
     const float ok = __shfl_down_sync(0xffffffffu, bk, off);
     const int32_t ov = __shfl_down_sync(0xffffffffu, bv, off);
+    float4 ol;
+    if (kNoise == 0) {
+      ol.x = __shfl_down_sync(0xffffffffu, bl.x, off);
+      ol.y = __shfl_down_sync(0xffffffffu, bl.y, off);
+      ol.z = __shfl_down_sync(0xffffffffu, bl.z, off);
+      ol.w = __shfl_down_sync(0xffffffffu, bl.w, off);
+    }
     merge_sums(m2, z, s1, om2, oz, os1);
     if (better(ok, ov, bk, bv)) {
       bk = ok;
       bv = ov;
+      if (kNoise == 0) bl = ol;
     }
   }
   if (lane == 0) {
@@ -582,6 +613,7 @@ __global__ void __launch_bounds__(kPassThreads, 3)
     red_f[warp][2] = s1;
     red_f[warp][3] = bk;
     red_v[warp] = bv;
+    red_l[warp] = bl;
   }
   __syncthreads();
   if (tid == 0) {
@@ -590,7 +622,18 @@ __global__ void __launch_bounds__(kPassThreads, 3)
       if (better(red_f[q][3], red_v[q], bk, bv)) {
         bk = red_f[q][3];
         bv = red_v[q];
+        bl = red_l[q];
       }
+    }
+    if (kNoise == 0) {
+      // the token inside the CTA's best group: groups of different CTAs are disjoint and
+      // the tokens of a lower group are lower, so (key, token) orders the partials as
+      // (key, group) did
+      const uint32_t g = static_cast<uint32_t>(bv);
+      uint32_t w[4];
+      philox4x32_10(group_counter(g), static_cast<uint32_t>(p), step, 1u, pk, w);
+      const uint32_t x = group_word(g) == 0 ? w[0] : group_word(g) == 1 ? w[1] : group_word(g) == 2 ? w[2] : w[3];
+      bv = static_cast<int32_t>(4 * g) + group_pick(bl, inv_temp, x);
     }
     Partial o;
     o.m2 = m2;
@@ -614,16 +657,17 @@ __device__ __forceinline__ float asc_dec(uint32_t u) {
 }
 
 __global__ void __launch_bounds__(kFinalThreads)
-    sample_final_kernel(const Partial* __restrict__ part, int P, int S, int rule, float bound, int noise,
-                        const float* __restrict__ logits, int64_t V, float inv_temp, uint32_t k0, uint32_t k1,
-                        uint32_t step,
+    sample_final_kernel(const Partial* __restrict__ part, int P, int S, int rule, float bound,
                         const uint8_t* __restrict__ revealed, int32_t* __restrict__ token, float* __restrict__ entropy,
                         float* __restrict__ pmax, uint8_t* __restrict__ accept) {
   __shared__ unsigned long long keys[kFinalThreads];  // rule 0: (entropy, position), sorted ascending
   __shared__ float red_pm[kFinalThreads / 32];
   __shared__ int red_q[kFinalThreads / 32];
   __shared__ uint8_t sh_acc[kFinalThreads];
-  grid_dependency_wait();  // the pass launch's partials
+  __shared__ __align__(16) float hs[kFinalThreads];  // rule 0: the sorted entropies
+  __shared__ __align__(16) float cs[kFinalThreads];  // and their running fp32 sums
+  grid_dependents_launch();  // the next call's pass may set up; it waits for this launch to finish
+  grid_dependency_wait();    // the pass launch's partials
   const int p = threadIdx.x, lane = p & 31, warp = p >> 5;
   float h = INFINITY, pm = 0.f;
   bool rev = true;  // positions past P take part as revealed
@@ -654,31 +698,7 @@ __global__ void __launch_bounds__(kFinalThreads)
     h = logf(z) - (s1 / z) * 0.693147180559945309f;
     pm = 1.f / z;
     rev = revealed[p] != 0;
-    // per group, the token inside the winning group: the first i whose running sum
-    // fl(..fl(e_0 + e_1).. + e_i) exceeds fl(U' S), U' from the group's word of its
-    // counter with fourth word 1; if none does, the last i with e_i > 0
-    if (noise == 0) {
-      const uint32_t g = static_cast<uint32_t>(bv);
-      const float4 l = __ldg(reinterpret_cast<const float4*>(logits + static_cast<int64_t>(p) * V) + g);
-      const GroupExp ge = group_exp(l, inv_temp);
-      uint32_t w[4];
-      philox4x32_10(group_counter(g), static_cast<uint32_t>(p), step, 1u, philox_keys(k0, k1), w);
-      const uint32_t x = w[group_word(g)];
-      const float u = __fmul_rn(__fadd_rn(static_cast<float>(x & 0x007fffffu), 0.5f), 0x1p-23f);
-      const float T = __fmul_rn(u, ge.s);
-      int pick = -1, last = 0;
-      float c = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        c = i == 0 ? ge.e[0] : __fadd_rn(c, ge.e[i]);
-        if (pick < 0 && c > T) pick = i;
-        if (ge.e[i] > 0.f) last = i;
-      }
-      token[p] = static_cast<int32_t>(4 * g) + (pick < 0 ? last : pick);
-    }
-    else {
-      token[p] = bv;
-    }
+    token[p] = bv;
     entropy[p] = h;
     pmax[p] = pm;
   }
@@ -722,45 +742,51 @@ __global__ void __launch_bounds__(kFinalThreads)
     // one fp32 rounding per step
     int n2 = 32;
     while (n2 < P) n2 <<= 1;
-    keys[p] = rev ? ~0ull : (static_cast<unsigned long long>(asc_enc(h)) << 32) | static_cast<uint32_t>(p);
+    unsigned long long key =
+        rev ? ~0ull : (static_cast<unsigned long long>(asc_enc(h)) << 32) | static_cast<uint32_t>(p);
     const int n = __syncthreads_count(!rev);
-    for (int k = 2; k <= n2; k <<= 1)
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        // a stage with j < 32 pairs lanes of one warp: the warp's own barrier orders it
-        if (j >= 32) __syncthreads();
-        const int q2 = p ^ j;
-        if (p < n2 && q2 > p) {
-          const unsigned long long a = keys[p], b = keys[q2];
-          if (((p & k) == 0) == (a > b)) {
-            keys[p] = b;
-            keys[q2] = a;
+    // thread p < n2 holds entry p; a stage pairs p with p ^ j, and the lower one of the
+    // pair keeps the smaller key where the k-block sorts ascending.  Pairs inside a warp
+    // (j < 32) swap through shuffles; the others through shared memory, ordered by a
+    // barrier of the n2 sorting threads alone (the warps past n2 hold no entries)
+    if (p < n2) {
+      for (int k = 2; k <= n2; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          unsigned long long other;
+          if (j < 32) {
+            other = __shfl_xor_sync(0xffffffffu, key, j);
+          } else {
+            keys[p] = key;
+            asm volatile("bar.sync 1, %0;" ::"r"(n2) : "memory");
+            other = keys[p ^ j];
+            asm volatile("bar.sync 1, %0;" ::"r"(n2) : "memory");
           }
+          const bool keep_min = ((p & k) == 0) == ((p & j) == 0);
+          key = keep_min ? (other < key ? other : key) : (other > key ? other : key);
         }
-        if (j >= 32) __syncthreads();
-        else __syncwarp();
-      }
+    }
+    // the rule in sorted order: c_i = fl(c_(i-1) + h_i) is the one sequential part (the
+    // order of the fp32 roundings is the rule's); the running maximum of ascending
+    // entropies is h_i itself.  Every thread decodes its entry, one thread runs the sums
+    // four entries at a time, then every thread decides its own entry
+    hs[p] = p < n ? asc_dec(static_cast<uint32_t>(key >> 32)) : 0.f;
     __syncthreads();
-    if (warp == 0) {
-      // warp 0 walks the sorted entries 32 at a time: lane u loads entry i0 + u, every
-      // lane runs the same sequence of fp32 sums and maxima over the broadcast values,
-      // and lane u keeps the decision for its own entry
-      float c = 0.f, x = -INFINITY;
-      for (int i0 = 0; i0 < n; i0 += 32) {
-        const unsigned long long kk = keys[min(i0 + lane, kFinalThreads - 1)];
-        const float hl = asc_dec(static_cast<uint32_t>(kk >> 32));
-        bool mine = false;
-#pragma unroll 8
-        for (int u = 0; u < 32; ++u) {
-          if (i0 + u >= n) break;
-          const float hu = __shfl_sync(0xffffffffu, hl, u);
-          c = __fadd_rn(c, hu);
-          x = fmaxf(x, hu);
-          const bool ok = i0 + u == 0 || __fsub_rn(c, x) <= bound;
-          if (u == lane) mine = ok;
-        }
-        if (mine && i0 + lane < n) sh_acc[static_cast<uint32_t>(kk)] = 1;
+    if (p == 0) {
+      // four entries per trip, the next four loaded ahead (hs is zero past n)
+      float c = 0.f;
+      float4 h4 = *reinterpret_cast<const float4*>(hs);
+      for (int i0 = 0; i0 < n; i0 += 4) {
+        const float4 nx = *reinterpret_cast<const float4*>(hs + min(i0 + 4, kFinalThreads - 4));
+        const float c0 = __fadd_rn(c, h4.x);
+        const float c1 = __fadd_rn(c0, h4.y);
+        const float c2 = __fadd_rn(c1, h4.z);
+        c = __fadd_rn(c2, h4.w);
+        *reinterpret_cast<float4*>(cs + i0) = make_float4(c0, c1, c2, c);
+        h4 = nx;
       }
     }
+    __syncthreads();
+    if (p < n && (p == 0 || __fsub_rn(cs[p], hs[p]) <= bound)) sh_acc[static_cast<uint32_t>(key)] = 1;
   }
   __syncthreads();
   if (p < P) accept[p] = sh_acc[p];
@@ -782,7 +808,7 @@ cudaError_t launch_sample(int P, int64_t V, float inv_temp, uint64_t seed, uint3
                                           chunk, inv_temp, k0, k1, step, part);
   if (e != cudaSuccess) return e;
   return launch_pdl(sample_final_kernel, dim3(1), dim3(kFinalThreads), 0, st, static_cast<const Partial*>(part), P, S,
-                    rule, bound, noise, logits, V, inv_temp, k0, k1, step, revealed, token, entropy, pmax, accept);
+                    rule, bound, revealed, token, entropy, pmax, accept);
 }
 
 }  // namespace moe
