@@ -40,12 +40,13 @@
 // instructions; per group, a Philox call serves sixteen elements and the screen runs
 // once per four, so the pass streams at memory speed.  Loads are streaming 16-byte
 // loads into registers, issued one to two iterations ahead; nothing waits on shared
-// memory or a barrier.  Each CTA writes its partial (m2, Z, S1, best key, token or group).
+// memory or a barrier.  Per group, the CTA reduction carries the best group's four
+// logits and thread 0 draws the token inside it (inverse CDF); each CTA writes its
+// partial (m2, Z, S1, best key, token).
 //
 // Final kernel (one CTA, one thread per position): merges each position's
 // partials in split order, writes entropy H = ln Z - (S1 / Z) ln 2, top-1
-// probability 1 / Z and the token (per group: the inverse-CDF pick inside the winning
-// group, from its four logits), then applies the acceptance rule to those fp32
+// probability 1 / Z and the token, then applies the acceptance rule to those fp32
 // values (entropy rule: a bitonic sort by (H, position), then one thread runs the
 // fp32 cumulative sum in sorted order and every thread decides its own entry).
 #include <cuda_runtime.h>
