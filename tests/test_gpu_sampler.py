@@ -175,3 +175,23 @@ def test_sampler_forms_sample_the_same_distribution(B):
             chi2 += (rest_o - rest_e) ** 2 / rest_e
             dof += 1
         assert chi2 < scipy_stats.chi2.ppf(1 - 1e-4, dof), (noise, chi2, dof)
+
+
+def test_sampler_random_shapes(B):
+    """Twelve seeded random configurations (positions 1..1024, vocabularies of 4..300,000
+    entries not aligned to any split, logits of scale 0.5..8, both rules, both noise
+    forms), every output checked against the oracle."""
+    rng = np.random.default_rng(2026)
+    for trial in range(12):
+        P = int(rng.choice([1, 2, 7, 33, 100, 257, 640, 1024]))
+        V = 4 * int(rng.integers(1, 75000 if P < 300 else 4000))
+        sigma = float(rng.choice([0.5, 1.0, 3.0, 8.0]))
+        inv_temp = float(np.float32(rng.uniform(0.4, 2.5)))
+        rule = int(rng.integers(0, 2))
+        bound = float(rng.uniform(0.0, 50.0)) if rule == 0 else float(rng.uniform(0.05, 0.95))
+        noise = trial % 2
+        seed, step = int(rng.integers(0, 2 ** 63)), int(rng.integers(0, 2 ** 32))
+        lg = _logits(P, V, sigma, seed=trial)
+        revealed = (rng.random(P) < 0.3).astype(np.uint8)
+        (got,) = _gpu_sample(B, lg, revealed, inv_temp, rule, bound, seed=seed, step=step, noise=noise)
+        _check(lg, revealed, inv_temp, rule, bound, seed, step, noise, got)
