@@ -16,10 +16,11 @@
 // operations and u rounds to nearest even, so u and the logits are reproducible
 // bit for bit off the GPU.
 //
-// One CTA per 8 tokens and 16 experts: warp w normalises token w into shared
+// One CTA per 8 tokens and 32 experts: warp w normalises token w into shared
 // memory (the CTAs of the first expert column also write u out), then each warp
-// forms the logits of two experts for the 8 tokens, each lane reusing one
-// 8-column chunk of the router row for all 8 tokens.
+// forms the logits of four experts for the 8 tokens in one pass over its lanes'
+// columns: a lane converts each 8-column chunk of u once and of each router row
+// once, and feeds all 32 (expert, token) sums from them.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -29,7 +30,8 @@ namespace moe {
 namespace {
 
 constexpr int kFrontTokens = 8;    // tokens per CTA (one warp each for the norm)
-constexpr int kFrontExperts = 16;  // experts per CTA (two per warp for the router)
+constexpr int kFrontExperts = 32;  // experts per CTA (four per warp for the router)
+constexpr int kWarpExperts = 4;
 constexpr int kFrontThreads = 256;
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
@@ -60,6 +62,17 @@ __global__ void __launch_bounds__(kFrontThreads) block_front_kernel(const uint16
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * kFrontTokens, e0 = blockIdx.y * kFrontExperts;
   const int nch = d / 8;
+  // the router rows of the warp's four experts; their first two chunks are loaded now, so
+  // that the loads overlap the pre-norm (rows past E read row E - 1 and are not written)
+  const int eb = e0 + kWarpExperts * warp;
+  const uint4* wrow[kWarpExperts];
+  uint4 wnext[kWarpExperts], wnext2[kWarpExperts];  // chunks c and c + 32 of the rows
+#pragma unroll
+  for (int j = 0; j < kWarpExperts; ++j) {
+    wrow[j] = reinterpret_cast<const uint4*>(wr + static_cast<size_t>(min(eb + j, E - 1)) * d);
+    wnext[j] = wrow[j][lane];
+    wnext2[j] = wrow[j][min(lane + 32, nch - 1)];
+  }
   {
     // ---- pre-norm of token t0 + warp
     const int t = t0 + warp;
@@ -67,6 +80,7 @@ __global__ void __launch_bounds__(kFrontThreads) block_front_kernel(const uint16
     if (t < T) {
       const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
       float ss = 0.f;
+#pragma unroll 8
       for (int c = lane; c < nch; c += 32) {
         const uint4 v = xr[c];
         srow[c] = v;
@@ -79,6 +93,7 @@ __global__ void __launch_bounds__(kFrontThreads) block_front_kernel(const uint16
       const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(d)), eps)));
       uint4* urow = reinterpret_cast<uint4*>(u_out + static_cast<size_t>(t) * d);
       const float4* g4 = reinterpret_cast<const float4*>(gamma);
+#pragma unroll 8
       for (int c = lane; c < nch; c += 32) {
         float f[8];
         unpack8(srow[c], f);
@@ -96,31 +111,38 @@ __global__ void __launch_bounds__(kFrontThreads) block_front_kernel(const uint16
     }
   }
   __syncthreads();
-  // ---- router logits of experts e0 + 2 warp + (0, 1) for the CTA's tokens
-  for (int j = 0; j < 2; ++j) {
-    const int e = e0 + 2 * warp + j;
-    if (e >= E) break;
-    const uint4* wrow = reinterpret_cast<const uint4*>(wr + static_cast<size_t>(e) * d);
-    float acc[kFrontTokens];
+  // ---- router logits of experts e0 + 4 warp + j (j < 4) for the CTA's tokens; each
+  // trip loads the chunk two ahead of the four rows before it uses the current one
+  float acc[kWarpExperts][kFrontTokens];
 #pragma unroll
-    for (int tt = 0; tt < kFrontTokens; ++tt) acc[tt] = 0.f;
-    for (int c = lane; c < nch; c += 32) {
-      float w[8];
-      unpack8(wrow[c], w);
+  for (int j = 0; j < kWarpExperts; ++j)
 #pragma unroll
-      for (int tt = 0; tt < kFrontTokens; ++tt) {
-        float uf[8];
-        unpack8(su[tt * nch + c], uf);
+    for (int tt = 0; tt < kFrontTokens; ++tt) acc[j][tt] = 0.f;
+  for (int c = lane; c < nch; c += 32) {
+    float w[kWarpExperts][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[tt] = fmaf(uf[i], w[i], acc[tt]);
-      }
+    for (int j = 0; j < kWarpExperts; ++j) {
+      unpack8(wnext[j], w[j]);
+      wnext[j] = wnext2[j];
+      if (c + 64 < nch) wnext2[j] = wrow[j][c + 64];
     }
 #pragma unroll
     for (int tt = 0; tt < kFrontTokens; ++tt) {
-      const float v = lane_butterfly_sum(acc[tt]);
-      if (lane == 0 && t0 + tt < T) logits[static_cast<size_t>(t0 + tt) * E + e] = v;
+      float uf[8];
+      unpack8(su[tt * nch + c], uf);
+#pragma unroll
+      for (int j = 0; j < kWarpExperts; ++j)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[j][tt] = fmaf(uf[i], w[j][i], acc[j][tt]);
     }
   }
+#pragma unroll
+  for (int j = 0; j < kWarpExperts; ++j)
+#pragma unroll
+    for (int tt = 0; tt < kFrontTokens; ++tt) {
+      const float v = lane_butterfly_sum(acc[j][tt]);
+      if (lane == 0 && eb + j < E && t0 + tt < T) logits[static_cast<size_t>(t0 + tt) * E + eb + j] = v;
+    }
 }
 
 }  // namespace
