@@ -508,8 +508,9 @@ def run_ours(args, rank, world, local):
                 "copies": "in and out on two copy streams, double-buffered: a step's copies overlap its neighbours' "
                           "computation; "
                           "the host loop calls the library and the CUDA runtime directly"},
-        # (pre-norm + router projection,) top-k, grouping, row copy, expert GEMMs, combine
-        "gpu_launches": K * layers * (6 if args.block else 5),
+        # (pre-norm + router projection,) top-k, grouping (two launches above 512 tokens), row copy,
+        # expert GEMMs, combine
+        "gpu_launches": K * layers * ((1 if args.block else 0) + (2 if wl.tokens <= 512 else 3) + 3),
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.block:
