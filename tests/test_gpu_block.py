@@ -113,3 +113,17 @@ def test_block_in_place_equals_separate_output(rt):
     a = _block_case(rt, wl, 9)
     b = _block_case(rt, wl, 9, in_place=True)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("fmt,red", [(1, 0), (2, 0), (0, 1), (1, 1), (2, 1)])
+def test_block_weight_formats_and_reduction_orders(rt, fmt, red):
+    """The block with affine-bias (1) and symmetric (2) weights and the group-factorised
+    order (reduction 1): same bars, the oracle dequantising the same format."""
+    import dataclasses
+    wl = dataclasses.replace(synth.WORKLOADS["tiny"], format=fmt, reduction=red)
+    _block_case(rt, wl, 11 + fmt + 3 * red)
+
+
+def test_block_256_experts_top8(rt):
+    """E = 256, k = 8 through the whole block (front, routing of its logits, layer, residual)."""
+    _block_case(rt, synth.Workload("e256", 9, 256, 64, 256, 8, 64, 32), 5)
