@@ -277,6 +277,9 @@ MOE_W4A16_API moe_w4a16_status moe_w4a16_block(const moe_w4a16_shape* shape, con
  *               rule 1 (confidence): revealed[p] == 0 and pmax[p] > bound; if no
  *               such position, the unrevealed one with the largest pmax (ties to
  *               the lower p).  Revealed positions are never accepted.
+ * Accuracy: entropy and pmax come from fp32 streaming sums; t2 = t log2 e is rounded
+ * once, so with T = max |t2| of a position their relative error is about 2e-5 +
+ * 2^-22 T (the tokens are exact at any scale).
  * Non-finite logits give unspecified (but in-bounds) results. */
 typedef struct {
   int32_t positions;      /* P, 1 .. 1024 */

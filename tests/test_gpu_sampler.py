@@ -195,3 +195,27 @@ def test_sampler_random_shapes(B):
         revealed = (rng.random(P) < 0.3).astype(np.uint8)
         (got,) = _gpu_sample(B, lg, revealed, inv_temp, rule, bound, seed=seed, step=step, noise=noise)
         _check(lg, revealed, inv_temp, rule, bound, seed, step, noise, got)
+
+
+@NOISE
+@pytest.mark.parametrize("sigma,inv_temp", [(50.0, 0.02), (50.0, 20.0), (0.01, 1.0), (0.5, 300.0)])
+def test_sampler_extreme_scales(B, sigma, inv_temp, noise):
+    """Logit scales and temperatures far from the workload's (t = logit * inv_temp from
+    ~1e-2 to ~1e4).  Tokens exact (the screen's margin scales with |m2| and |K| and must
+    never drop the winning token) and acceptance equal to the rule on the GPU's values.
+    Entropy and confidence get a bar derived from the fp32 arithmetic: t2 = fl(logit *
+    fl(inv_temp log2 e)) is off by up to 2^-23 |t2|, so with T = max |t2| every
+    probability is off by a relative ~2^-22 T; pmax within 2e-5 + 2^-22 T relative,
+    the entropy within (2e-5 + 2^-22 T)(H + 1)."""
+    P, V = 12, 50000
+    lg = _logits(P, V, sigma, seed=int(sigma * 100) + int(inv_temp))
+    revealed = (np.arange(P) % 4 == 0).astype(np.uint8)
+    (got,) = _gpu_sample(B, lg, revealed, inv_temp, 0, 5.0, seed=31, step=2, noise=noise)
+    tok, ent, pm, acc = got
+    o_tok, o_ent, o_pm = oracle.sample(lg, inv_temp, 31, 2, nthreads=NCPU, noise=noise)
+    assert np.array_equal(tok, o_tok), np.nonzero(tok != o_tok)[0][:10]
+    T = float(np.abs(lg.astype(np.float64)).max()) * inv_temp * 1.4426950408889634
+    rel = 2e-5 + 2.0 ** -22 * T
+    assert np.all(np.abs(pm.astype(np.float64) - o_pm) <= rel * o_pm), float(np.abs(pm / o_pm - 1).max())
+    assert np.all(np.abs(ent.astype(np.float64) - o_ent) <= rel * (np.abs(o_ent) + 1)), float(np.abs(ent - o_ent).max())
+    assert np.array_equal(acc, oracle.accept_entropy(ent, revealed, 5.0))
